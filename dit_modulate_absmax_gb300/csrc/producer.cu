@@ -1,0 +1,503 @@
+// producer.cu -- the two-pass NVFP4 activation producer for sm_103a.
+//
+// Pass 1 ("NVFP4 Modulation Producer Fusion", Dataflow, prototype step 1;
+// "NVFP4 Streaming Design", Numerical Constraint items 1-2): re-derive the
+// bf16 producer values y (AdaLN modulation, or BF16 SwiGLU for the FC2 input),
+// reduce one exact global max |y| and turn it into the FP32 tensor scale.
+//
+// Pass 2 (prototype step 2; Numerical Constraint items 3-4): re-derive the same
+// y, compute one E4M3 block scale per 16 values and the E2M1 codes, and write
+// packed QDATA plus the scales directly in the GEMM's 128x4-atom scale layout.
+//
+// Both passes walk the activation in tiles of 128 rows x 256 columns.  A warp
+// reads one 512-byte row segment per instruction (16 bytes per lane), so every
+// load is a full, coalesced 128-byte line set; lanes 2i and 2i+1 hold the two
+// halves of one 16-value block.  A pass-2 tile produces exactly four scale
+// atoms (2 KB, contiguous in the scale layout), which are assembled in shared
+// memory and written with 16-byte stores.  Pass 2 walks the tiles in the
+// reverse of pass 1's order so that its first tiles are the ones pass 1 read
+// last, which are still resident in L2.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace h3fp4 {
+namespace {
+
+// kSiluLut: uint16[65536], the correctly rounded bf16 silu of every bf16
+// pattern (generated at build time); used where the FP32 evaluation below is
+// too close to a bf16 rounding boundary, and for g < -80 and NaN.
+#include "silu_lut.inc"
+
+constexpr int kTileRows = 128;
+constexpr int kTileCols = 256;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowsPerWarp = kTileRows / kWarps;  // 16
+constexpr int kUnroll = 4;                         // rows in flight per lane
+
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u)
+{
+    __nv_bfloat162 r;
+    memcpy(&r, &u, 4);
+    return r;
+}
+
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v)
+{
+    uint32_t r;
+    memcpy(&r, &v, 4);
+    return r;
+}
+
+// Correctly rounded bf16x2 multiply and add (no contraction into an FMA).
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) { return as_u32(__hmul2_rn(as_bf2(a), as_bf2(b))); }
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) { return as_u32(__hadd2_rn(as_bf2(a), as_bf2(b))); }
+
+__device__ __forceinline__ uint4 ld16(const uint16_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+// Segment of row r and its row range [begin, end): s is the number of
+// interior boundaries off[1..nseg-1] at or below r (offsets are
+// non-decreasing), begin the largest of off[0..nseg-1] at or below r, end the
+// smallest of off[1..nseg] above r.  Fully unrolled with constant indices so
+// that the table stays in kernel-parameter space.
+__device__ __forceinline__ int segment_of(const SegTable &t, int64_t r, int64_t &begin, int64_t &end)
+{
+    int s = 0;
+    begin = 0;
+    end = INT64_MAX;
+#pragma unroll
+    for (int i = 1; i <= H3FP4_MAX_SEGMENTS; ++i) {
+        const int64_t v = t.off[i];
+        const bool valid = i <= t.nseg;
+        const bool interior = i < t.nseg;
+        s += (interior && r >= v) ? 1 : 0;
+        begin = (interior && r >= v && v > begin) ? v : begin;
+        end = (valid && v > r && v < end) ? v : end;
+    }
+    return s;
+}
+
+// Exact value of an E4M3 code with the sign bit clear (bias 7, 3 mantissa bits).
+__device__ __forceinline__ float e4m3_value(uint32_t c)
+{
+    const uint32_t e = (c >> 3) & 0xFu, mant = c & 7u;
+    return e ? __uint_as_float(((e + 120u) << 23) | (mant << 20)) : static_cast<float>(mant) * 0.001953125f;
+}
+
+// Correctly rounded bf16 silu(g) = g / (1 + e^-g) for one bf16 pattern.
+// FP32 evaluation: expf (at most 2 ulp) then a correctly rounded add and
+// divide leave a relative error below 2^-21, i.e. a few fp32 ulps; when the 16
+// bits below the bf16 rounding point are within 64 of the halfway pattern the
+// rounding is not certain and the table decides.  For g >= -80 the result is a
+// normal fp32 number, so the ulp argument holds.
+__device__ __forceinline__ uint32_t silu_bf16(uint32_t gbits)
+{
+    const float g = __uint_as_float(gbits << 16);
+    if (!(g >= -80.0f))
+        return kSiluLut[gbits];
+    const float e = expf(-g);
+    const float s = __fdiv_rn(g, __fadd_rn(1.0f, e));
+    const uint32_t u = __float_as_uint(s);
+    if ((u & 0xFFFFu) - 0x7FC0u <= 0x80u)
+        return kSiluLut[gbits];
+    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+// ---------------------------------------------------------------------------
+// Sources of the producer values y, 8 consecutive bf16 per lane and row.
+// ---------------------------------------------------------------------------
+struct ModulateSrc {
+    const uint16_t *x;
+    int64_t ldx;
+    const uint16_t *shift;
+    const uint16_t *scale;
+    int64_t ld_mod;
+    SegTable seg;
+
+    using Raw = uint4;
+    struct State {
+        int64_t begin, end;  // rows of the segment whose parameters are loaded
+        uint32_t s1[4], sh[4];
+    };
+
+    __device__ __forceinline__ void begin(State &st) const
+    {
+        st.begin = 1;
+        st.end = 0;  // empty range: the first row loads its segment
+    }
+    __device__ __forceinline__ Raw load(int64_t r, int col) const { return ld16(x + r * ldx + col); }
+
+    // y = RN_bf16(RN_bf16(x * RN_bf16(scale + 1)) + shift), per segment of row r.
+    __device__ __forceinline__ void apply(State &st, int64_t r, int col, const Raw &raw, uint32_t (&y)[4]) const
+    {
+        if (r < st.begin || r >= st.end) {
+            const int s = segment_of(seg, r, st.begin, st.end);
+            const uint4 sc = ld16(scale + s * ld_mod + col);
+            const uint4 sh = ld16(shift + s * ld_mod + col);
+            const uint32_t one2 = 0x3F803F80u;  // bf16 1.0 in both halves
+            st.s1[0] = bf2_add(sc.x, one2);
+            st.s1[1] = bf2_add(sc.y, one2);
+            st.s1[2] = bf2_add(sc.z, one2);
+            st.s1[3] = bf2_add(sc.w, one2);
+            st.sh[0] = sh.x;
+            st.sh[1] = sh.y;
+            st.sh[2] = sh.z;
+            st.sh[3] = sh.w;
+        }
+        y[0] = bf2_add(bf2_mul(raw.x, st.s1[0]), st.sh[0]);
+        y[1] = bf2_add(bf2_mul(raw.y, st.s1[1]), st.sh[1]);
+        y[2] = bf2_add(bf2_mul(raw.z, st.s1[2]), st.sh[2]);
+        y[3] = bf2_add(bf2_mul(raw.w, st.s1[3]), st.sh[3]);
+    }
+    __device__ __forceinline__ void keep(int64_t, int, const uint32_t (&)[4]) const {}
+};
+
+struct SwigluSrc {
+    const uint16_t *g;
+    int64_t ldg;
+    const uint16_t *u;
+    int64_t ldu;
+    uint16_t *h;  // optional output of pass 1 (leading dimension ldh)
+    int64_t ldh;
+
+    struct Raw {
+        uint4 g, u;
+    };
+    struct State {};
+
+    __device__ __forceinline__ void begin(State &) const {}
+    __device__ __forceinline__ Raw load(int64_t r, int col) const
+    {
+        return Raw{ld16(g + r * ldg + col), ld16(u + r * ldu + col)};
+    }
+
+    // h = RN_bf16(silu_bf16(gate) * up).
+    __device__ __forceinline__ void apply(State &, int64_t, int, const Raw &raw, uint32_t (&y)[4]) const
+    {
+        const uint32_t gw[4] = {raw.g.x, raw.g.y, raw.g.z, raw.g.w};
+        const uint32_t uw[4] = {raw.u.x, raw.u.y, raw.u.z, raw.u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t s = silu_bf16(gw[i] & 0xFFFFu) | (silu_bf16(gw[i] >> 16) << 16);
+            y[i] = bf2_mul(s, uw[i]);
+        }
+    }
+    __device__ __forceinline__ void keep(int64_t r, int col, const uint32_t (&y)[4]) const
+    {
+        if (h)
+            *reinterpret_cast<uint4 *>(h + r * ldh + col) = make_uint4(y[0], y[1], y[2], y[3]);
+    }
+};
+
+struct PlainSrc {  // already-materialised bf16 values (SwiGLU pass 2 with a workspace)
+    const uint16_t *h;
+    int64_t ldh;
+
+    using Raw = uint4;
+    struct State {};
+    __device__ __forceinline__ void begin(State &) const {}
+    __device__ __forceinline__ Raw load(int64_t r, int col) const { return ld16(h + r * ldh + col); }
+    __device__ __forceinline__ void apply(State &, int64_t, int, const Raw &raw, uint32_t (&y)[4]) const
+    {
+        y[0] = raw.x;
+        y[1] = raw.y;
+        y[2] = raw.z;
+        y[3] = raw.w;
+    }
+    __device__ __forceinline__ void keep(int64_t, int, const uint32_t (&)[4]) const {}
+};
+
+__device__ __forceinline__ uint32_t absmax8(const uint32_t (&y)[4])
+{
+    uint32_t v = __vmaxu2(__vmaxu2(y[0] & 0x7FFF7FFFu, y[1] & 0x7FFF7FFFu),
+                          __vmaxu2(y[2] & 0x7FFF7FFFu, y[3] & 0x7FFF7FFFu));
+    return max(v & 0xFFFFu, v >> 16);
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1: global absmax and tensor scale.  Persistent grid; each CTA folds its
+// maximum into scratch[0] with one atomicMax, and the last CTA to finish
+// (counted in scratch[1]) converts the maximum into the tensor scale.
+// ---------------------------------------------------------------------------
+template <class Src>
+__global__ void __launch_bounds__(kThreads) absmax_kernel(Src src, int64_t m, int col_tiles, int64_t n_tiles,
+                                                          uint32_t *scratch, float *ts_out)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    typename Src::State st;
+    uint32_t vmax = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int64_t row0 = (t / col_tiles) * kTileRows;
+        const int col = static_cast<int>(t % col_tiles) * kTileCols + lane * 8;
+        src.begin(st);  // cached per-column parameters belong to the previous tile's columns
+#pragma unroll 1
+        for (int i0 = 0; i0 < kRowsPerWarp; i0 += kUnroll) {
+            typename Src::Raw raw[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t r = row0 + warp + kWarps * (i0 + u);
+                if (r < m)
+                    raw[u] = src.load(r, col);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t r = row0 + warp + kWarps * (i0 + u);
+                if (r < m) {
+                    uint32_t y[4];
+                    src.apply(st, r, col, raw[u], y);
+                    src.keep(r, col, y);
+                    vmax = max(vmax, absmax8(y));
+                }
+            }
+        }
+    }
+    vmax = __reduce_max_sync(0xFFFFFFFFu, vmax);
+    __shared__ uint32_t wmax[kWarps];
+    if (lane == 0)
+        wmax[warp] = vmax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t mx = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            mx = max(mx, wmax[w]);
+        atomicMax(&scratch[0], mx);
+        __threadfence();
+        const uint32_t done = atomicAdd(&scratch[1], 1u);
+        if (done == gridDim.x - 1) {
+            __threadfence();
+            const uint32_t a = atomicOr(&scratch[0], 0u);
+            // ts = RN_f32(amax / (6 * 448)); a NaN maximum (pattern above 0x7F80) stays NaN.
+            *ts_out = __fdiv_rn(__uint_as_float(a << 16), 2688.0f);
+        }
+    }
+}
+
+// True when q (>= 0) lies within 32 fp32 ulps of a number with at most three
+// significant bits.  Every E2M1 rounding midpoint (0.25, 0.75, 1.25, 1.75,
+// 2.5, 3.5, 5) is such a number.
+__device__ __forceinline__ bool near_short_value(float q)
+{
+    return ((__float_as_uint(q) + 32u) & 0x1FFFFFu) < 64u;
+}
+
+// E2M1 codes of 8 values with the block's FP32 scale product sc; byte i holds
+// element 2i in its low nibble.  A zero scale product gives signed zeros.
+//
+// The code of y is E2M1_RNE_sat(RN_f32(y / sc)); the sign is taken from y and
+// the magnitude rounded from |y|.  Instead of one IEEE division per value the
+// block computes r = RN(1/sc) once and q = RN(|y| * r), which differs from the
+// exact quotient by less than 2^-22 (relative).  The E2M1 rounding of q and of
+// RN_f32(|y| / sc) can only differ when a midpoint lies within that distance,
+// i.e. when q is within 8 ulps of a midpoint; any q within 32 ulps of a
+// three-significant-bit number is recomputed with the IEEE division.  Scale
+// products outside [2^-125, 2^125], whose reciprocal is not a normal number,
+// always take the division.
+__device__ __forceinline__ uint32_t encode8(const uint32_t (&y)[4], float sc)
+{
+    uint32_t signs = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        signs |= (((y[i] >> 12) & 0x8u) | ((y[i] >> 24) & 0x80u)) << (8 * i);
+    if (sc == 0.0f)
+        return signs;
+    float a[8], q[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        a[2 * i] = __uint_as_float((y[i] & 0x7FFFu) << 16);
+        a[2 * i + 1] = __uint_as_float(y[i] & 0x7FFF0000u);
+    }
+    bool slow = !(sc >= 0x1p-125f && sc <= 0x1p125f);
+    if (!slow) {
+        const float r = __frcp_rn(sc);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            q[e] = __fmul_rn(a[e], r);
+            slow |= near_short_value(q[e]);
+        }
+    }
+    if (slow) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            q[e] = __fdiv_rn(a[e], sc);
+    }
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        out |= cvt_e2m1x2(q[2 * i + 1], q[2 * i]) << (8 * i);
+    return out | signs;
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: one CTA per 128 x 256 tile (tiles visited in reverse order).
+// ---------------------------------------------------------------------------
+template <class Src>
+__global__ void __launch_bounds__(kThreads) pack_kernel(Src src, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
+                                                        int64_t n_tiles, const float *ts_ptr, uint8_t *qdata,
+                                                        uint8_t *sf)
+{
+    __shared__ __align__(16) uint8_t sft[4 * 512];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = n_tiles - 1 - blockIdx.x;
+    const int64_t row_tile = t / col_tiles;
+    const int col_tile = static_cast<int>(t % col_tiles);
+    const int64_t row0 = row_tile * kTileRows;
+    const int col = col_tile * kTileCols + lane * 8;
+    const int64_t qld = d / 2;
+    const float ts = *ts_ptr;
+    const float den = __fmul_rn(6.0f, ts);
+    typename Src::State st;
+    src.begin(st);
+
+#pragma unroll 1
+    for (int i0 = 0; i0 < kRowsPerWarp; i0 += kUnroll) {
+        typename Src::Raw raw[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t r = row0 + warp + kWarps * (i0 + u);
+            if (r < m)
+                raw[u] = src.load(r, col);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int rr = warp + kWarps * (i0 + u);
+            const int64_t r = row0 + rr;
+            uint32_t y[4] = {0u, 0u, 0u, 0u};
+            if (r < m)
+                src.apply(st, r, col, raw[u], y);
+            const uint32_t a = absmax8(y);
+            const uint32_t bmax = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+            // bs = E4M3_RNE_sat(RN_f32(block_amax / RN_f32(6 ts))); an all-zero block gets 0.
+            const uint32_t bs = bmax ? cvt_e4m3(__fdiv_rn(__uint_as_float(bmax << 16), den)) : 0u;
+            const float sc = __fmul_rn(e4m3_value(bs), ts);
+            const uint32_t packed = encode8(y, sc);
+            if (r < m_pad)
+                *reinterpret_cast<uint32_t *>(qdata + r * qld + col / 2) = packed;
+            if ((lane & 1) == 0) {
+                const int b = lane >> 1;  // block within the tile, 0..15
+                sft[(b >> 2) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (b & 3)] = static_cast<uint8_t>(bs);
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        const int64_t atoms_per_row_tile = d / 64;
+        uint8_t *dst = sf + (row_tile * atoms_per_row_tile + col_tile * 4) * 512;
+        reinterpret_cast<uint4 *>(dst)[threadIdx.x] = reinterpret_cast<const uint4 *>(sft)[threadIdx.x];
+    }
+}
+
+// Logical [rows, cols] (leading dimension ld) -> 128x4-atom scale layout.
+__global__ void swizzle_kernel(const uint8_t *src, int64_t rows, int64_t cols, int64_t ld, uint8_t *dst,
+                               int64_t total)
+{
+    for (int64_t o = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o < total;
+         o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t atom = o / 512, within = o % 512;
+        const int64_t atoms_per_row_tile = cols / 4;
+        const int64_t r = (atom / atoms_per_row_tile) * 128 + (within / 16) + ((within % 16) / 4) * 32;
+        const int64_t c = (atom % atoms_per_row_tile) * 4 + (within % 4);
+        dst[o] = r < rows ? src[r * ld + c] : 0;
+    }
+}
+
+template <class Src>
+cudaError_t run_absmax(const Src &src, int64_t m, int64_t d, float *ts, uint32_t *scratch, cudaStream_t st)
+{
+    if (m == 0)
+        return cudaMemsetAsync(ts, 0, sizeof(float), st);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), st);
+    if (e != cudaSuccess)
+        return e;
+    const int col_tiles = static_cast<int>(d / kTileCols);
+    const int64_t n_tiles = ((m + kTileRows - 1) / kTileRows) * col_tiles;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+    const int grid = static_cast<int>(n_tiles < cap ? n_tiles : cap);
+    absmax_kernel<Src><<<grid, kThreads, 0, st>>>(src, m, col_tiles, n_tiles, scratch, ts);
+    return cudaGetLastError();
+}
+
+template <class Src>
+cudaError_t run_pack(const Src &src, int64_t m, int64_t m_pad, int64_t d, const float *ts, uint8_t *qdata,
+                     uint8_t *sf, cudaStream_t st)
+{
+    const int col_tiles = static_cast<int>(d / kTileCols);
+    const int64_t row_tiles = (m_pad + kTileRows - 1) / kTileRows;
+    const int64_t n_tiles = row_tiles * col_tiles;
+    if (n_tiles == 0)
+        return cudaSuccess;
+    if (n_tiles > 0x7FFFFFFF)
+        return cudaErrorInvalidValue;
+    pack_kernel<Src><<<static_cast<unsigned>(n_tiles), kThreads, 0, st>>>(src, m, m_pad, d, col_tiles, n_tiles, ts,
+                                                                           qdata, sf);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 148;
+    if (cached[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+cudaError_t launch_modulate_absmax(const uint16_t *x, int64_t ldx, int64_t m, int64_t d, const uint16_t *shift,
+                                   const uint16_t *scale, int64_t ld_mod, const SegTable &seg, float *ts,
+                                   uint32_t *scratch, cudaStream_t st)
+{
+    ModulateSrc src{x, ldx, shift, scale, ld_mod, seg};
+    return run_absmax(src, m, d, ts, scratch, st);
+}
+
+cudaError_t launch_modulate_pack(const uint16_t *x, int64_t ldx, int64_t m, int64_t m_pad, int64_t d,
+                                 const uint16_t *shift, const uint16_t *scale, int64_t ld_mod, const SegTable &seg,
+                                 const float *ts, uint8_t *qdata, uint8_t *sf, cudaStream_t st)
+{
+    ModulateSrc src{x, ldx, shift, scale, ld_mod, seg};
+    return run_pack(src, m, m_pad, d, ts, qdata, sf, st);
+}
+
+cudaError_t launch_swiglu_pack(const uint16_t *gate, int64_t ldg, const uint16_t *up, int64_t ldu, int64_t m,
+                               int64_t m_pad, int64_t f, float *ts, uint32_t *scratch, uint8_t *qdata, uint8_t *sf,
+                               uint16_t *h, cudaStream_t st)
+{
+    SwigluSrc src{gate, ldg, up, ldu, h, f};
+    cudaError_t e = run_absmax(src, m, f, ts, scratch, st);
+    if (e != cudaSuccess)
+        return e;
+    if (h != nullptr && m > 0) {
+        PlainSrc plain{h, f};
+        return run_pack(plain, m, m_pad, f, ts, qdata, sf, st);
+    }
+    SwigluSrc recompute{gate, ldg, up, ldu, nullptr, f};
+    return run_pack(recompute, m, m_pad, f, ts, qdata, sf, st);
+}
+
+cudaError_t launch_swizzle_scales(const uint8_t *src, int64_t rows, int64_t cols, int64_t ld, uint8_t *dst,
+                                  cudaStream_t st)
+{
+    const int64_t total = ((rows + 127) / 128) * 128 * cols;
+    if (total == 0)
+        return cudaSuccess;
+    const int64_t blocks = (total + 255) / 256;
+    const int grid = static_cast<int>(blocks < 4096 ? blocks : 4096);
+    swizzle_kernel<<<grid, 256, 0, st>>>(src, rows, cols, ld, dst, total);
+    return cudaGetLastError();
+}
+
+}  // namespace h3fp4

@@ -1,0 +1,77 @@
+"""Runs one hot-path call on synthetic inputs, for profilers.
+
+  python -m dit_modulate_absmax_gb300.profile_case {modulate,swiglu,gemm} [--m M] [--n N] [--k K] [--reps R]
+
+`modulate` runs both passes of the modulation producer on an [M, K]
+activation, `swiglu` the SwiGLU producer on [M, K] gate/up, `gemm` the
+block-scaled GEMM of a packed [M, K] activation with a packed [N, K] weight.
+The R timed repetitions run between cudaProfilerStart and cudaProfilerStop
+(so `ncu --profile-from-start off` sees only them) after two warm-up calls,
+and the mean CUDA-event time per call is printed.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+
+import torch
+
+import dit_modulate_absmax_gb300 as h3
+from dit_modulate_absmax_gb300 import build as B
+from dit_modulate_absmax_gb300 import workloads as W
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op", choices=("modulate", "swiglu", "gemm"))
+    ap.add_argument("--m", type=int, default=W.M_TOKENS)
+    ap.add_argument("--n", type=int, default=21504)
+    ap.add_argument("--k", type=int, default=7168)
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args()
+    B.build()
+    dev = torch.device("cuda")
+    m_pad = -(-a.m // 16) * 16
+    base = W.WORKLOADS["fc2" if a.op == "swiglu" else "qkv"]
+    w = dataclasses.replace(base, m=a.m, m_pad=m_pad, k=a.k, n=a.n,
+                            seg_off=(0, min(32768, a.m), a.m) if base.kind == "modulate" else ())
+    act = W.activations(w, device=dev)
+    off = W.seg_offsets(w)
+    ts = torch.empty(1, dtype=torch.float32, device=dev)
+    scratch = torch.empty(2, dtype=torch.int32, device=dev)
+    q = torch.empty(m_pad, a.k // 2, dtype=torch.uint8, device=dev)
+    sfa = torch.empty(h3.sf_bytes(m_pad, a.k), dtype=torch.uint8, device=dev)
+    if a.op == "swiglu":
+        def call():
+            h3.swiglu_pack(act["gate"], act["up"], m_pad, tensor_scale=ts, scratch=scratch, qdata=q, sfa=sfa)
+    else:
+        def produce():
+            h3.modulate_absmax(act["x"], act["shift"], act["scale"], off, tensor_scale=ts, scratch=scratch)
+            h3.modulate_pack(act["x"], act["shift"], act["scale"], off, ts, m_pad, qdata=q, sfa=sfa)
+        call = produce
+        if a.op == "gemm":
+            produce()
+            wt = W.weights(w, device=dev)
+            bsf = h3.swizzle_scales(wt["sf"][: a.n])
+            bts = torch.tensor([wt["ts"]], dtype=torch.float32, device=dev)
+            c = torch.empty(a.m, a.n, dtype=torch.int16, device=dev)
+
+            def call():
+                h3.gemm(q, sfa, ts, wt["q"], bsf, bts, a.m, out=c)
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.profiler.start()
+    e0.record()
+    for _ in range(a.reps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    assert h3.h3fp4_device_error() == 0
+    print(f"{a.op} m={a.m} n={a.n} k={a.k}: {e0.elapsed_time(e1) / a.reps:.4f} ms per call")
+
+
+if __name__ == "__main__":
+    main()

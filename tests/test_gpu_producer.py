@@ -1,0 +1,235 @@
+"""GPU parity of the two-pass NVFP4 producers against the CPU oracle.
+
+The tensor scale, every QDATA byte and every scale byte (compared after the
+oracle applies its own scale layout) must match bit for bit.  Output buffers
+are pre-filled with a canary so that a byte the kernels fail to write shows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dit_modulate_absmax_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+CANARY = 0xAB
+
+
+def _u16(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+def _to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def _f32_bits(v):
+    return int(np.float32(v).view(np.uint32))
+
+
+def run_modulate(h3, x, sh, sc, off, m_pad, x_dev=None):
+    m, d = x.shape
+    xd = _to_dev(x) if x_dev is None else x_dev
+    shd, scd = _to_dev(sh), _to_dev(sc)
+    q = torch.full((m_pad, d // 2), CANARY, dtype=torch.uint8, device="cuda")
+    sfa = torch.full((h3.sf_bytes(m_pad, d),), CANARY, dtype=torch.uint8, device="cuda")
+    ts = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    h3.modulate_absmax(xd, shd, scd, off, tensor_scale=ts)
+    h3.modulate_pack(xd, shd, scd, off, ts, m_pad, qdata=q, sfa=sfa)
+    torch.cuda.synchronize()
+    assert h3.h3fp4_device_error() == 0
+    return float(ts.item()), q.cpu().numpy(), sfa.cpu().numpy()
+
+
+def check_modulate(h3, x, sh, sc, off, m_pad):
+    ts_o, q_o, sf_o, _, _ = oracle.modulate_producer(x, sh, sc, off, m_pad)
+    ts, q, sfa = run_modulate(h3, x, sh, sc, off, m_pad)
+    assert _f32_bits(ts) == _f32_bits(ts_o), (ts, ts_o)
+    assert np.array_equal(q, q_o), f"QDATA differs at {np.argwhere(q != q_o)[:5].tolist()}"
+    want = oracle.swizzle_sf(sf_o)
+    assert np.array_equal(sfa, want), f"SFA differs at {np.argwhere(sfa != want)[:5].tolist()}"
+    return ts
+
+
+def _bf16(t):
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _random_case(m, d, nseg, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = _bf16(torch.randn(m, d, generator=g) * scale)
+    sh = _bf16(torch.randn(nseg, d, generator=g) * 0.2)
+    sc = _bf16(torch.randn(nseg, d, generator=g) * 0.2)
+    return x, sh, sc
+
+
+def test_tiny_adversarial_bit_exact(h3):
+    from oracle.adversarial import tiny_adversarial
+    w = W.WORKLOADS["tiny"]
+    a = W.activations(w)
+    off = W.seg_offsets(w)
+    sh = a["shift"].numpy().view(np.uint16)
+    sc = a["scale"].numpy().view(np.uint16)
+    x = tiny_adversarial(a["x"].numpy().view(np.uint16), sh, sc, off)
+    ts = check_modulate(h3, x, sh, sc, off, w.m_pad)
+    assert ts == 4.0
+
+
+def test_tiny_plain_bit_exact(h3):
+    w = W.WORKLOADS["tiny"]
+    a = W.activations(w)
+    check_modulate(h3, _u16(a["x"]), _u16(a["shift"]), _u16(a["scale"]), W.seg_offsets(w), w.m_pad)
+
+
+@pytest.mark.parametrize("m,m_pad,d,off", [
+    (1, 16, 256, [0, 1]),
+    (129, 144, 512, [0, 100, 129]),
+    (300, 320, 768, [0, 0, 150, 300]),            # empty first segment
+    (1000, 1024, 256, [0, 200, 200, 700, 1000]),  # empty middle segment
+    (257, 384, 256, [0, 257]),                    # m_pad well past m
+    (640, 640, 1024, [0, 128, 256, 384, 512, 640]),
+])
+def test_ragged_shapes_bit_exact(h3, m, m_pad, d, off):
+    x, sh, sc = _random_case(m, d, len(off) - 1, seed=m + d)
+    check_modulate(h3, x, sh, sc, off, m_pad)
+
+
+def test_ctas_walking_several_tiles_bit_exact(h3):
+    """Pass 1 runs a capped persistent grid: at this size every CTA walks several
+    tiles in different column slabs, with the largest |y| in a late tile."""
+    m, d = 16384 + 77, 4096                    # 129 x 16 = 2064 tiles, more than the grid
+    x, sh, sc = _random_case(m, d, 2, seed=18)
+    x[16300, 3000] = oracle.bf16_bits(900.0)   # the global maximum, far from the first tiles
+    check_modulate(h3, x, sh, sc, [0, 9000, m], m + 3)
+
+
+def test_many_segments_bit_exact(h3):
+    m, d = 700, 256
+    off = list(range(0, 700, 50)) + [700]          # 14 segments of 50 rows
+    x, sh, sc = _random_case(m, d, len(off) - 1, seed=21)
+    check_modulate(h3, x, sh, sc, off, 704)
+
+
+def test_wide_dynamic_range_and_subnormals(h3):
+    rng = np.random.default_rng(12)
+    m, d = 200, 512
+    mag = 10.0 ** rng.uniform(-40, 30, size=(m, d))
+    x = _bf16(torch.from_numpy(mag * rng.choice([-1.0, 1.0], size=(m, d))).float())
+    x[5] = rng.integers(1, 0x80, size=d).astype(np.uint16)            # subnormal x
+    x[6] = x[5] | 0x8000
+    x[7] = 0x8000                                                       # -0 row
+    sh = _bf16(torch.randn(1, d) * 1e-20)
+    sc = _bf16(torch.randn(1, d) * 0.5)
+    check_modulate(h3, x, sh, sc, [0, m], 208)
+
+
+def test_small_amax_tensor(h3):
+    # every value tiny: tensor scale in the fp32 subnormal range, block scales saturate or vanish
+    m, d = 64, 256
+    x, sh, sc = _random_case(m, d, 1, seed=13, scale=1e-36)
+    sh[:] = 0
+    check_modulate(h3, x, sh, sc, [0, m], 64)
+
+
+def test_zero_rows_gives_zero_scale(h3):
+    d, m_pad = 256, 32
+    x = np.zeros((0, d), dtype=np.uint16)
+    sh = np.zeros((1, d), dtype=np.uint16)
+    xd = torch.zeros((1, d), dtype=torch.int16, device="cuda")[:0]
+    ts, q, sfa = run_modulate(h3, x, sh, sh, [0, 0], m_pad, x_dev=xd)
+    assert ts == 0.0 and not q.any() and not sfa.any()
+
+
+def test_all_zero_tensor(h3):
+    m, d = 50, 256
+    x = np.zeros((m, d), dtype=np.uint16)
+    x[3, 7] = 0x8000
+    sh = np.zeros((1, d), dtype=np.uint16)
+    ts = check_modulate(h3, x, sh, sh, [0, m], 64)
+    assert ts == 0.0
+
+
+def test_nan_input_gives_nan_scale_without_error(h3):
+    m, d = 20, 256
+    x, sh, sc = _random_case(m, d, 1, seed=14)
+    x[4, 9] = 0x7FC0
+    ts, _, _ = run_modulate(h3, x, sh, sc, [0, m], 32)
+    assert np.isnan(ts)
+
+
+def test_leading_dimensions(h3):
+    m, d, ldx, ldm = 100, 256, 384, 264
+    g = torch.Generator().manual_seed(15)
+    xw = torch.randn(m, ldx, generator=g).to(torch.bfloat16).view(torch.int16)
+    shw = (torch.randn(2, ldm, generator=g) * 0.2).to(torch.bfloat16).view(torch.int16)
+    scw = (torch.randn(2, ldm, generator=g) * 0.2).to(torch.bfloat16).view(torch.int16)
+    off = [0, 60, 100]
+    ts_o, q_o, sf_o, _, _ = oracle.modulate_producer(_u16(xw[:, :d].contiguous()), _u16(shw[:, :d].contiguous()),
+                                                     _u16(scw[:, :d].contiguous()), off, 112)
+    xd, shd, scd = xw.cuda()[:, :d], shw.cuda()[:, :d], scw.cuda()[:, :d]
+    ts = h3.modulate_absmax(xd, shd, scd, off)
+    q, sfa = h3.modulate_pack(xd, shd, scd, off, ts, 112)
+    torch.cuda.synchronize()
+    assert float(ts.item()) == ts_o
+    assert np.array_equal(q.cpu().numpy(), q_o)
+    assert np.array_equal(sfa.cpu().numpy(), oracle.swizzle_sf(sf_o))
+
+
+def test_repeated_calls_are_deterministic(h3):
+    x, sh, sc = _random_case(500, 512, 2, seed=16)
+    a = run_modulate(h3, x, sh, sc, [0, 300, 500], 512)
+    b = run_modulate(h3, x, sh, sc, [0, 300, 500], 512)
+    assert a[0] == b[0] and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU producer
+# ---------------------------------------------------------------------------
+def run_swiglu(h3, g, u, m_pad, workspace):
+    m, f = g.shape
+    gd, ud = _to_dev(g), _to_dev(u)
+    hw = torch.full((m, f), 0x5555, dtype=torch.int16, device="cuda") if workspace else None
+    q = torch.full((m_pad, f // 2), CANARY, dtype=torch.uint8, device="cuda")
+    sfa = torch.full((h3.sf_bytes(m_pad, f),), CANARY, dtype=torch.uint8, device="cuda")
+    ts, q, sfa = h3.swiglu_pack(gd, ud, m_pad, h_workspace=hw, qdata=q, sfa=sfa)
+    torch.cuda.synchronize()
+    assert h3.h3fp4_device_error() == 0
+    return float(ts.item()), q.cpu().numpy(), sfa.cpu().numpy(), (None if hw is None else _u16(hw))
+
+
+def test_silu_exhaustive_over_all_bf16_gates(h3):
+    """h = silu_bf16(g) * 1 for every one of the 65,536 bf16 gate patterns."""
+    g = np.arange(65536, dtype=np.uint16).reshape(256, 256)
+    u = np.full((256, 256), 0x3F80, dtype=np.uint16)         # up = 1.0
+    _, _, _, h = run_swiglu(h3, g, u, 256, workspace=True)
+    want = oracle.silu_table().reshape(256, 256)
+    nan_w = (want & 0x7FFF) > 0x7F80
+    nan_h = (h & 0x7FFF) > 0x7F80
+    assert np.array_equal(nan_h, nan_w)
+    bad = np.argwhere((h != want) & ~nan_w)
+    assert bad.size == 0, [(hex(int(g[i, j])), hex(int(h[i, j])), hex(int(want[i, j]))) for i, j in bad[:8]]
+
+
+@pytest.mark.parametrize("workspace", [False, True])
+@pytest.mark.parametrize("m,m_pad,f,scale", [(64, 64, 256, 1.0), (300, 320, 512, 3.0), (129, 256, 768, 20.0)])
+def test_swiglu_bit_exact(h3, m, m_pad, f, scale, workspace):
+    gen = torch.Generator().manual_seed(m + f)
+    g = _bf16(torch.randn(m, f, generator=gen) * scale)
+    u = _bf16(torch.randn(m, f, generator=gen))
+    ts_o, q_o, sf_o, h_o, _ = oracle.swiglu_producer(g, u, m_pad)
+    ts, q, sfa, h = run_swiglu(h3, g, u, m_pad, workspace)
+    assert _f32_bits(ts) == _f32_bits(ts_o)
+    assert np.array_equal(q, q_o)
+    assert np.array_equal(sfa, oracle.swizzle_sf(sf_o))
+    if workspace:
+        assert np.array_equal(h, h_o)
+
+
+def test_swizzle_kernel_matches_oracle_layout(h3):
+    rng = np.random.default_rng(17)
+    for rows, cols in [(384, 16), (300, 64), (1, 4), (129, 896)]:
+        sf = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+        got = h3.swizzle_scales(torch.from_numpy(sf).cuda()).cpu().numpy()
+        pad = np.zeros((h3.sf_rows(rows), cols), dtype=np.uint8)
+        pad[:rows] = sf
+        assert np.array_equal(got, oracle.swizzle_sf(pad))
