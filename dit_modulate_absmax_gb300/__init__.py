@@ -29,6 +29,7 @@ _SIGNATURES = {
     "h3fp4_swiglu_pack": ([_P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P], _STATUS),
     "h3fp4_gemm": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P], _STATUS),
     "h3fp4_swizzle_scales": ([_P, _I64, _I64, _I64, _P, _P], _STATUS),
+    "h3fp4_swiglu_pack_noalloc": ([_P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P], _STATUS),
     "h3fp4_device_error": ([_P], _STATUS),
     "h3fp4_status_string": ([_STATUS], ctypes.c_char_p),
     "h3fp4_build_info": ([], ctypes.c_char_p),
@@ -112,6 +113,14 @@ def h3fp4_gemm(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg: Ge
 
 def h3fp4_swizzle_scales(sf_logical, rows, cols, ld, sf_out, stream=0):
     _call("h3fp4_swizzle_scales", sf_logical, rows, cols, ld, sf_out, stream)
+
+
+def h3fp4_swiglu_pack_noalloc(gate, ldg, up, ldu, m, m_pad, f, tensor_scale, qdata, sfa, stream=0):
+    """The SwiGLU producer with library-owned static scratch, for callers that cannot allocate."""
+    _call("h3fp4_swiglu_pack_noalloc", gate, ldg, up, ldu, m, m_pad, f, tensor_scale, qdata, sfa, stream)
+
+
+NOALLOC_MAX_ELEMENTS = 1 << 22
 
 
 def h3fp4_device_error() -> int:

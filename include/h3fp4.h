@@ -188,6 +188,37 @@ H3FP4_API h3fp4_status h3fp4_swizzle_scales(const uint8_t *sf_logical, int64_t r
                                   int64_t ld, uint8_t *sf_out, void *stream);
 
 /*
+ * h3fp4_swiglu_pack_noalloc -- h3fp4_swiglu_pack for callers that cannot
+ * allocate device memory.  No counterpart on the source pages.
+ *
+ * Some callers have no device allocator at hand when they call in (a plugin
+ * running inside another framework's operator, a serving loop that must not
+ * allocate after warm-up), so they cannot pass the scratch words or the h
+ * workspace.  This entry point computes exactly what h3fp4_swiglu_pack
+ * computes (same tensor scale, QDATA and SFA bytes) with its scratch in a
+ * static device array owned by the library: 256 bytes of counters plus room
+ * for H3FP4_NOALLOC_MAX_ELEMENTS bf16 values of h (8 MiB in all), held by
+ * every GPU that loads the library until the process exits.  It calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *
+ *   Arguments as for h3fp4_swiglu_pack, without scratch and h_workspace.
+ *   m * f must not exceed H3FP4_NOALLOC_MAX_ELEMENTS (else H3FP4_ERR_SHAPE,
+ *   nothing enqueued).
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and may load the library's device code; make that first
+ * call before any stream capture.  All calls share the array and it keeps the
+ * last call's contents (each call clears its counters and rewrites h before
+ * reading it); calls whose GPU work overlaps race on it and must be
+ * serialised by the caller.
+ */
+#define H3FP4_NOALLOC_MAX_ELEMENTS (1 << 22)
+H3FP4_API h3fp4_status h3fp4_swiglu_pack_noalloc(const void *gate_bf16, int64_t ldg, const void *up_bf16,
+                                                 int64_t ldu, int64_t m, int64_t m_pad, int64_t f,
+                                                 float *tensor_scale, uint8_t *qdata, uint8_t *sfa,
+                                                 void *stream);
+
+/*
  * h3fp4_device_error -- reads and clears the device-side error word of the
  * current device (synchronous).  Kernels whose pipeline waits give up after
  * their time limit record a nonzero code there instead of hanging.
