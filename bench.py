@@ -143,6 +143,26 @@ def _profile_traffic(linear):
 
 
 # ----------------------------------------------------------------------------
+# ranks: N replicas, one per GPU, no collective on the data path
+# ----------------------------------------------------------------------------
+def max_over_ranks(value_ms: float, device=None) -> float:
+    """Largest value over all ranks (the job's time is its slowest replica's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value_ms)
+    t = torch.tensor([float(value_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_ms_per_linear(step_ms: float, linears_per_step: int, world: int) -> float:
+    """Whole-job milliseconds per linear: every rank runs its own block, so the
+    job finishes linears_per_step * world linears per (slowest) step."""
+    return step_ms / (linears_per_step * world)
+
+
+# ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
 def _bytes_per_element(kind):
@@ -240,11 +260,7 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.profiler.stop()
     if world > 1:
         dist.barrier()
-    elapsed_ms = start.elapsed_time(stop)
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), dev)
     assert h3.h3fp4_device_error() == 0
 
     per = {}
@@ -277,17 +293,14 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e_stop.record()
     torch.cuda.synchronize()
-    e_ms = torch.tensor([e_start.elapsed_time(e_stop)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
-    e_ms = float(e_ms.item())
+    e_ms = max_over_ranks(e_start.elapsed_time(e_stop), dev)
 
     if rank != 0:
         return None
     peaks = _peaks()
     fp4_peak = peaks["bf16_sustained"] * FP4_PER_BF16
     ms_per_step = elapsed_ms / args.steps
-    value = ms_per_step / (len(lins) * world)
+    value = job_ms_per_linear(ms_per_step, len(lins), world)
     kernels = {}
     for L in lins:
         p = per[L.name]
@@ -315,7 +328,7 @@ def run_ours(args, rank, world, local_rank):
                                     f"{FP4_PER_BF16:g} (nominal NVFP4/BF16 ratio)"},
         "kernels": kernels,
         "hbm_peak_gbs": peaks["hbm_gbs"],
-        "e2e": {"value": round(e_ms / args.steps / (len(lins) * world), 4), "unit": UNIT,
+        "e2e": {"value": round(job_ms_per_linear(e_ms / args.steps, len(lins), world), 4), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": sum(L.launches for L in lins) * args.steps,
         "clocks": clocks,

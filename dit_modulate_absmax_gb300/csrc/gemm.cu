@@ -11,12 +11,17 @@
 //               the A tile (128 rows x 128 bytes) and the B tile (256 x 128 bytes),
 //               both with 128-byte swizzle, plus 1-D bulk copies of the scale
 //               atoms (A: 4 atoms = 2 KB, B: 2 x 2 KB), into a 4-stage ring;
-//   warp 1      allocates TMEM, then one lane copies the scale atoms into TMEM
-//               (tcgen05.cp 32x128b.warpx4) and issues four
+//   warp 1      allocates TMEM, then one lane issues four
 //               tcgen05.mma kind::mxf4nvf4 (K = 64 each) per stage into the
 //               FP32 accumulator (TMEM columns 0-255); tcgen05.commit frees the
 //               stage and, after a tile's last stage, hands the accumulator to
 //               the epilogue;
+//   warps 10-13 scale warps, one per TMEM lane quarter: once a stage has
+//               landed they move its scale atoms from shared memory into TMEM
+//               with tcgen05.st (the MMA's scale layout) and arrive on the
+//               stage's sf_ready barrier, which the MMA lane waits on.  (Copying
+//               the atoms with tcgen05.cp instead costs twelve tensor-pipe
+//               instructions per stage, which measured as the main limiter.)
 //   warps 2-9   epilogue: each warp drains one 32-lane quarter x 128 columns of
 //               the accumulator into registers (tcgen05.ld), releases the
 //               accumulator at once so that the next tile's MMAs can start, and
@@ -25,8 +30,9 @@
 // M-tiles with N fastest, so every 128-row A tile is used by n_group
 // consecutive tiles while it is L2-resident, and the B tiles of a group stay
 // resident while the group sweeps M (the N-group A-tile reuse factor).
-// The scale copies of stage s live in their own 48 TMEM columns (256 + 48 s),
-// so a later stage never overwrites scales an in-flight MMA still reads.
+// The scales of stage s live in their own 48 TMEM columns (256 + 48 s), so a
+// later stage never overwrites scales an in-flight MMA still reads (the scale
+// warps refill stage s only after its loads, which follow the MMAs' commit).
 // Every pipeline wait gives up after 2 s and records a device error instead of
 // hanging.
 #include <cuda.h>
@@ -58,8 +64,11 @@ constexpr uint32_t ATOM = 512;           // 128 rows x 4 scales
 constexpr uint32_t SFA_BYTES = 4 * ATOM; // 128 rows x 16 scales
 constexpr uint32_t SFB_BYTES = 8 * ATOM; // 256 rows x 16 scales
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kDefaultNGroup = 16;
+constexpr int kScaleWarps = 4;                     // one per TMEM lane quarter
+constexpr int kFirstEpiWarp = 2;
+constexpr int kFirstScaleWarp = kFirstEpiWarp + kEpiWarps;
+constexpr int kThreads = 32 * (2 + kEpiWarps + kScaleWarps);
+constexpr int kDefaultNGroup = 28;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SF_COL = 256;
@@ -71,14 +80,17 @@ constexpr uint32_t ERR_WAIT_EMPTY = 1u;
 constexpr uint32_t ERR_WAIT_FULL = 2u;
 constexpr uint32_t ERR_WAIT_ACC = 4u;
 constexpr uint32_t ERR_WAIT_ACC_EMPTY = 8u;
+constexpr uint32_t ERR_WAIT_SCALES = 16u;
 
 struct __align__(1024) Smem {
     uint8_t a[kStages][A_BYTES];
     uint8_t b[kStages][B_BYTES];
     uint8_t sfa[kStages][SFA_BYTES];
     uint8_t sfb[kStages][SFB_BYTES];
-    uint64_t full[kStages];
+    uint64_t full[kStages];      // A and B tiles landed
+    uint64_t sf_full[kStages];   // scale atoms landed
     uint64_t empty[kStages];
+    uint64_t sf_ready[kStages];  // scales staged in TMEM
     uint64_t acc_full;
     uint64_t acc_empty;
     uint32_t tmem_base;
@@ -94,6 +106,48 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n)
 }
 
 __device__ __forceinline__ void record_error(uint32_t code) { atomicOr(&g_device_error, code); }
+
+// Bounded wait by every lane of a warp; the outcome is made warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
+{
+    const bool ok = mbar_wait_bounded(bar, parity, kWaitLimitNs);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// Moves one stage's scale atoms from shared memory into TMEM, in the layout
+// the block-scaled MMA reads: for MMA K step j, row i (16 bytes) of the
+// 128x4 atom goes to columns 4j .. 4j+3 of lane 32q + i for every lane
+// quarter q, i.e. the layout of a tcgen05.cp .32x128b.warpx4 copy of the atom.
+// SFA (4 atoms, one per K step) lands at sfa_col (16 columns); SFB (two
+// 128-row halves x 4 atoms) at sfb_col (32 columns: step j, half h at 8j + 4h).
+// Executed by a whole warp; `lane_base` selects the warp's lane quarter.
+// One tcgen05.st per operand replaces twelve tcgen05.cp in the tensor pipe.
+__device__ __forceinline__ void stage_scales(uint32_t lane_base, uint32_t sfa_col, uint32_t sfb_col,
+                                             const uint8_t *sfa, const uint8_t *sfb, int lane)
+{
+    uint32_t a[16], b[32];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(sfa + j * ATOM + lane * 16);
+        a[4 * j + 0] = v.x;
+        a[4 * j + 1] = v.y;
+        a[4 * j + 2] = v.z;
+        a[4 * j + 3] = v.w;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(sfb + h * (4 * ATOM) + j * ATOM + lane * 16);
+            b[8 * j + 4 * h + 0] = v.x;
+            b[8 * j + 4 * h + 1] = v.y;
+            b[8 * j + 4 * h + 2] = v.z;
+            b[8 * j + 4 * h + 3] = v.w;
+        }
+    tmem_st_32x32b_x16(lane_base + sfa_col, a);
+    tmem_st_32x32b_x32(lane_base + sfb_col, b);
+    tmem_st_wait();
+}
 
 // Output tile t of the persistent schedule: groups of n_group N-tiles x all
 // M-tiles, N fastest inside a group (the last group may be narrower).
@@ -124,7 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.sf_full[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), 1);
+            mbar_init(smem_u32(&sm.sf_ready[s]), kScaleWarps);
         }
         mbar_init(smem_u32(&sm.acc_full), 1);
         mbar_init(smem_u32(&sm.acc_empty), kEpiWarps);
@@ -149,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int mt, nt;
                 tile_coords(t, m_tiles, n_tiles, n_group, mt, nt);
                 const bool has_rb1 = (2 * nt + 1) < n_rb;   // second 128-row half of the B tile exists
-                const uint32_t tx = A_BYTES + B_BYTES + SFA_BYTES + (has_rb1 ? SFB_BYTES : SFB_BYTES / 2);
+                const uint32_t sf_tx = SFA_BYTES + (has_rb1 ? SFB_BYTES : SFB_BYTES / 2);
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
@@ -158,16 +214,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t bar = smem_u32(&sm.full[s]);
-                    mbar_arrive_expect_tx(bar, tx);
-                    tma_load_2d(smem_u32(sm.a[s]), &tmA, kt * BKB, mt * BM, bar);
-                    tma_load_2d(smem_u32(sm.b[s]), &tmB, kt * BKB, nt * BN, bar);
-                    bulk_load(smem_u32(sm.sfa[s]), a_sf + (mt * atoms_per_rb + kt * 4) * ATOM, SFA_BYTES, bar);
+                    // scales first (small; the scale warps stage them while A and B are in flight)
+                    const uint32_t sbar = smem_u32(&sm.sf_full[s]);
+                    mbar_arrive_expect_tx(sbar, sf_tx);
+                    bulk_load(smem_u32(sm.sfa[s]), a_sf + (mt * atoms_per_rb + kt * 4) * ATOM, SFA_BYTES, sbar);
                     bulk_load(smem_u32(sm.sfb[s]), b_sf + ((2 * nt) * atoms_per_rb + kt * 4) * ATOM, SFB_BYTES / 2,
-                              bar);
+                              sbar);
                     if (has_rb1)
                         bulk_load(smem_u32(sm.sfb[s]) + SFB_BYTES / 2,
-                                  b_sf + ((2 * nt + 1) * atoms_per_rb + kt * 4) * ATOM, SFB_BYTES / 2, bar);
+                                  b_sf + ((2 * nt + 1) * atoms_per_rb + kt * 4) * ATOM, SFB_BYTES / 2, sbar);
+                    const uint32_t bar = smem_u32(&sm.full[s]);
+                    mbar_arrive_expect_tx(bar, A_BYTES + B_BYTES);
+                    tma_load_2d(smem_u32(sm.a[s]), &tmA, kt * BKB, mt * BM, bar);
+                    tma_load_2d(smem_u32(sm.b[s]), &tmB, kt * BKB, nt * BN, bar);
                 }
             }
         }
@@ -186,7 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
-                    if (!mbar_wait_bounded(smem_u32(&sm.full[s]), ph, kWaitLimitNs)) {
+                    // A and B landed, and the scale warps have put this stage's scales in TMEM
+                    if (!mbar_wait_bounded(smem_u32(&sm.full[s]), ph, kWaitLimitNs) ||
+                        !mbar_wait_bounded(smem_u32(&sm.sf_ready[s]), ph, kWaitLimitNs)) {
                         record_error(ERR_WAIT_FULL);
                         ok = false;
                         break;
@@ -194,15 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t sfa_t = tmem + SF_COL + s * SF_COLS_PER_STAGE;
                     const uint32_t sfb_t = sfa_t + 16;
-                    const uint32_t sfa_s = smem_u32(sm.sfa[s]);
-                    const uint32_t sfb_s = smem_u32(sm.sfb[s]);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(sfa_s + j * ATOM, 0, 128, 0));
-                        tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(sfb_s + j * ATOM, 0, 128, 0));
-                        tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4,
-                                             smem_desc(sfb_s + SFB_BYTES / 2 + j * ATOM, 0, 128, 0));
-                    }
                     const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, 1024, 2);
                     const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, 1024, 2);
 #pragma unroll
@@ -217,9 +269,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_commit(smem_u32(&sm.acc_full));
             }
         }
+    } else if (warp >= kFirstScaleWarp) {
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+            bool ok = true;
+            for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                if (!warp_wait(smem_u32(&sm.sf_full[s]), ph)) {
+                    if (lane == 0)
+                        record_error(ERR_WAIT_SCALES);
+                    ok = false;
+                    break;
+                }
+                stage_scales(tmem + lane_base, SF_COL + s * SF_COLS_PER_STAGE, SF_COL + s * SF_COLS_PER_STAGE + 16,
+                             sm.sfa[s], sm.sfb[s], lane);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&sm.sf_ready[s]));
+            }
+            if (!ok)
+                break;
+        }
     } else {
-        const int q = warp & 3;              // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;    // which 128 accumulator columns it drains
+        const int q = warp & 3;                          // TMEM lane quarter this warp may access
+        const int half = (warp - kFirstEpiWarp) >> 2;    // which 128 accumulator columns it drains
         const float alpha = __fmul_rn(*a_ts, *b_ts);
         uint32_t local = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
@@ -236,12 +312,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t v[4][32];
+            // Drain 32 columns at a time, applying alpha and rounding to bf16 at
+            // once, so that only the packed half-width results stay live.
+            uint32_t pk[64];
             const uint32_t base = tmem + (static_cast<uint32_t>(q * 32) << 16) + ACC_COL + half * 128;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tmem_ld_32x32b_x32(base + 32 * c, v[c]);
-            tmem_ld_wait();
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(base + 32 * c, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float lo = __fmul_rn(alpha, __uint_as_float(v[2 * i]));
+                    const float hi = __fmul_rn(alpha, __uint_as_float(v[2 * i + 1]));
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                    memcpy(&pk[16 * c + i], &b2, 4);
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
@@ -252,20 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row < m && col0 < n) {
                 uint4 *dst = reinterpret_cast<uint4 *>(C + static_cast<int64_t>(row) * ldc + col0);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t p[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float lo = __fmul_rn(alpha, __uint_as_float(v[c][2 * i]));
-                        const float hi = __fmul_rn(alpha, __uint_as_float(v[c][2 * i + 1]));
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-                        memcpy(&p[i], &b2, 4);
-                    }
-                    dst[4 * c + 0] = make_uint4(p[0], p[1], p[2], p[3]);
-                    dst[4 * c + 1] = make_uint4(p[4], p[5], p[6], p[7]);
-                    dst[4 * c + 2] = make_uint4(p[8], p[9], p[10], p[11]);
-                    dst[4 * c + 3] = make_uint4(p[12], p[13], p[14], p[15]);
-                }
+                for (int i = 0; i < 16; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
         }
     }
@@ -277,6 +352,250 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, TMEM_COLS);
     }
 }
+
+// ---------------------------------------------------------------------------
+// CTA-pair variant (tcgen05 cta_group::2).  A cluster of two CTAs on two SMs
+// computes a 256 x 256 output tile: each CTA loads its own 128 rows of A and
+// its own 128 rows (output columns) of B per K step, plus its 128 rows of A
+// scales and all 256 rows of B scales; the leader CTA (rank 0) issues the pair
+// MMA (M = 256) whose accumulator rows 0-127 land in the leader's TMEM and
+// rows 128-255 in the peer's.  Per SM and K step this moves 38 KB instead of
+// 54 KB for the same MMA work, so the ring holds 5 stages.
+//   - Both CTAs' A and B loads complete on the leader's full barrier (the
+//     peer's through the cta_group::2 form of the tensor copy).  Each CTA's
+//     scale atoms complete on its own sf_full barrier; its scale warps stage
+//     them in its own TMEM and arrive on the leader's sf_ready barrier (8
+//     arrivals: 4 warps x 2 CTAs).  The MMA thread waits on full and sf_ready.
+//   - The leader's commits arrive on the barrier of both CTAs (multicast):
+//     a stage is free in both CTAs once the pair's MMAs have read it.
+//   - Each CTA's epilogue drains its own accumulator rows and arrives on the
+//     leader's accumulator-empty barrier (16 arrivals: 8 warps x 2 CTAs).
+// ---------------------------------------------------------------------------
+namespace pair {
+
+constexpr int BM = 128;                    // rows per CTA; the pair covers 256
+constexpr int BN = 256;                    // output columns per pair tile
+constexpr int kStages = 5;
+constexpr uint32_t A_BYTES = BM * BKB;     // 16 KB
+constexpr uint32_t B_BYTES = 128 * BKB;    // 16 KB: this CTA's half of the B tile
+constexpr uint32_t SFA_BYTES = 4 * ATOM;   // this CTA's 128 rows x 16 scales
+constexpr uint32_t SFB_BYTES = 8 * ATOM;   // all 256 B rows x 16 scales
+constexpr uint32_t SF_ROW = 256;           // row length of the scale tensor maps
+
+struct __align__(1024) Smem {
+    uint8_t a[kStages][A_BYTES];
+    uint8_t b[kStages][B_BYTES];
+    uint8_t sfa[kStages][SFA_BYTES];
+    uint8_t sfb[kStages][SFB_BYTES];
+    uint64_t full[kStages];      // leader: both CTAs' A and B tiles landed
+    uint64_t sf_full[kStages];   // this CTA's scale atoms landed
+    uint64_t empty[kStages];     // both CTAs, arrived by the leader's commits
+    uint64_t sf_ready[kStages];  // leader: both CTAs' scales staged in TMEM
+    uint64_t acc_full;           // both CTAs
+    uint64_t acc_empty;          // used in the leader
+    uint32_t tmem_base;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                          const float *__restrict__ a_ts, const float *__restrict__ b_ts, uint16_t *__restrict__ C,
+                          int64_t ldc, int m, int n, int k, int m_tiles2, int n_tiles, int n_group, int sfa_rbs,
+                          int sfb_rbs)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+    const int kt_count = k / BK;
+    const int chunks_per_rb = k / 256;          // 2 KB scale chunks per 128-row block
+    const int total_tiles = m_tiles2 * n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.sf_full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
+            mbar_init(smem_u32(&sm.sf_ready[s]), 2 * kScaleWarps);
+        }
+        mbar_init(smem_u32(&sm.acc_full), 1);
+        mbar_init(smem_u32(&sm.acc_empty), 2 * kEpiWarps);
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmSFA);
+        prefetch_tmap(&tmSFB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&sm.tmem_base), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = pair_id; t < total_tiles && ok; t += num_pairs) {
+                int mt2, nt;
+                tile_coords(t, m_tiles2, n_tiles, n_group, mt2, nt);
+                const int rb_a = 2 * mt2 + static_cast<int>(rank);
+                const bool has_sfa = rb_a < sfa_rbs;   // else every row of this half is padding
+                const bool has_b1 = 2 * nt + 1 < sfb_rbs;
+                const uint32_t sf_tx = (has_sfa ? SFA_BYTES : 0u) + (has_b1 ? SFB_BYTES : SFB_BYTES / 2);
+                for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ph ^ 1u, kWaitLimitNs)) {
+                        record_error(ERR_WAIT_EMPTY);
+                        ok = false;
+                        break;
+                    }
+                    // scales first, on this CTA's own barrier (its scale warps stage them)
+                    const uint32_t sbar = smem_u32(&sm.sf_full[s]);
+                    mbar_arrive_expect_tx(sbar, sf_tx);
+                    if (has_sfa)
+                        tma_load_2d(smem_u32(sm.sfa[s]), &tmSFA, 0, (rb_a * chunks_per_rb + kt) * 8, sbar);
+                    tma_load_2d(smem_u32(sm.sfb[s]), &tmSFB, 0, (2 * nt * chunks_per_rb + kt) * 8, sbar);
+                    if (has_b1)
+                        tma_load_2d(smem_u32(sm.sfb[s]) + SFB_BYTES / 2, &tmSFB, 0,
+                                    ((2 * nt + 1) * chunks_per_rb + kt) * 8, sbar);
+                    // A and B halves of both CTAs complete on the leader's full barrier
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(smem_u32(&sm.full[s]), 2 * (A_BYTES + B_BYTES));
+                    const uint32_t bar = mapa_shared(smem_u32(&sm.full[s]), 0);
+                    tma_load_2d_pair(smem_u32(sm.a[s]), &tmA, kt * BKB, mt2 * 256 + static_cast<int>(rank) * 128, bar);
+                    tma_load_2d_pair(smem_u32(sm.b[s]), &tmB, kt * BKB, nt * BN + static_cast<int>(rank) * 128, bar);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_nvf4(2 * BM, BN);
+            uint32_t it = 0, local = 0;
+            bool ok = true;
+            for (int t = pair_id; t < total_tiles && ok; t += num_pairs, ++local) {
+                if (!mbar_wait_bounded(smem_u32(&sm.acc_empty), (local & 1) ^ 1u, kWaitLimitNs)) {
+                    record_error(ERR_WAIT_ACC_EMPTY);
+                    break;
+                }
+                tc_fence_after();
+                for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    // both CTAs' A and B landed and both CTAs' scales are in TMEM
+                    if (!mbar_wait_bounded(smem_u32(&sm.full[s]), ph, kWaitLimitNs) ||
+                        !mbar_wait_bounded(smem_u32(&sm.sf_ready[s]), ph, kWaitLimitNs)) {
+                        record_error(ERR_WAIT_FULL);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + SF_COL + s * SF_COLS_PER_STAGE;
+                    const uint32_t sfb_t = sfa_t + 16;
+                    const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, 1024, 2);
+                    const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, 1024, 2);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tc_mma_nvf4_pair(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, idesc, sfa_t + 4 * j,
+                                         sfb_t + 8 * j, (kt | j) != 0);
+                    tc_commit_pair_mc(smem_u32(&sm.empty[s]), 0x3);
+                }
+                if (ok)
+                    tc_commit_pair_mc(smem_u32(&sm.acc_full), 0x3);
+            }
+        }
+    } else if (warp >= kFirstScaleWarp) {
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        uint32_t it = 0;
+        for (int t = pair_id; t < total_tiles; t += num_pairs) {
+            bool ok = true;
+            for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                if (!warp_wait(smem_u32(&sm.sf_full[s]), ph)) {
+                    if (lane == 0)
+                        record_error(ERR_WAIT_SCALES);
+                    ok = false;
+                    break;
+                }
+                stage_scales(tmem + lane_base, SF_COL + s * SF_COLS_PER_STAGE, SF_COL + s * SF_COLS_PER_STAGE + 16,
+                             sm.sfa[s], sm.sfb[s], lane);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&sm.sf_ready[s]), 0));
+            }
+            if (!ok)
+                break;
+        }
+    } else {
+        const int q = warp & 3;
+        const int half = (warp - kFirstEpiWarp) >> 2;
+        const float alpha = __fmul_rn(*a_ts, *b_ts);
+        const uint32_t leader_acc_empty = mapa_shared(smem_u32(&sm.acc_empty), 0);
+        uint32_t local = 0;
+        for (int t = pair_id; t < total_tiles; t += num_pairs, ++local) {
+            int mt2, nt;
+            tile_coords(t, m_tiles2, n_tiles, n_group, mt2, nt);
+            bool ok = false;
+            if (lane == 0)
+                ok = mbar_wait_bounded(smem_u32(&sm.acc_full), local & 1, kWaitLimitNs);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            __syncwarp();
+            if (!ok) {
+                if (lane == 0)
+                    record_error(ERR_WAIT_ACC);
+                break;
+            }
+            tc_fence_after();
+            // Drain 32 columns at a time, applying alpha and rounding to bf16 at
+            // once, so that only the packed half-width results stay live.
+            uint32_t pk[64];
+            const uint32_t base = tmem + (static_cast<uint32_t>(q * 32) << 16) + ACC_COL + half * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(base + 32 * c, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float lo = __fmul_rn(alpha, __uint_as_float(v[2 * i]));
+                    const float hi = __fmul_rn(alpha, __uint_as_float(v[2 * i + 1]));
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                    memcpy(&pk[16 * c + i], &b2, 4);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)   // this CTA's rows are drained (relaxed: earlier tiles' stores need not land first)
+                mbar_arrive_cluster_relaxed(leader_acc_empty);
+
+            const int row = mt2 * 256 + static_cast<int>(rank) * BM + q * 32 + lane;
+            const int col0 = nt * BN + half * 128;
+            if (row < m && col0 < n) {
+                uint4 *dst = reinterpret_cast<uint4 *>(C + static_cast<int64_t>(row) * ldc + col0);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync();   // no CTA leaves while its peer may still touch its barriers or TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace pair
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -310,15 +629,81 @@ bool make_operand_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t k
     return r == CUDA_SUCCESS;
 }
 
+// 2-D uint8 tensor map viewing a scale buffer of `bytes` bytes as rows of 256
+// bytes, box 256 x 8 (one 2 KB chunk = 4 scale atoms), no swizzle.
+bool make_scale_map(CUtensorMap *tm, const void *base, int64_t bytes)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(pair::SF_ROW), static_cast<cuuint64_t>(bytes / pair::SF_ROW)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(pair::SF_ROW)};
+    cuuint32_t box[2] = {pair::SF_ROW, 8};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+h3fp4_status launch_pair(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
+                         const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m, int64_t m_pad,
+                         int64_t n, int64_t k, int n_group_cfg, cudaStream_t st)
+{
+    const int64_t sfa_rows = (m_pad + 127) / 128 * 128, sfb_rows = (n + 127) / 128 * 128;
+    CUtensorMap tmA, tmB, tmSFA, tmSFB;
+    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, pair::BM) || !make_operand_map(&tmB, b_q, n, k / 2, 128) ||
+        !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16)) || !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16)))
+        return H3FP4_ERR_CUDA;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return H3FP4_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(pair::nvf4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(pair::kSmemBytes)) != cudaSuccess)
+            return H3FP4_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    const int m_tiles2 = static_cast<int>((m + 255) / 256);
+    const int n_tiles = static_cast<int>((n + pair::BN - 1) / pair::BN);
+    const int64_t total = static_cast<int64_t>(m_tiles2) * n_tiles;
+    if (total > 0x7FFFFFFF)
+        return H3FP4_ERR_SHAPE;
+    int n_group = n_group_cfg > 0 ? n_group_cfg : kDefaultNGroup;
+    if (n_group > n_tiles)
+        n_group = n_tiles;
+    const int max_pairs = sm_count() / 2;
+    const int pairs = static_cast<int>(total < max_pairs ? total : max_pairs);
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(2 * pairs, 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = pair::kSmemBytes;
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&lc, pair::nvf4_gemm_pair_kernel, tmA, tmB, tmSFA, tmSFB, a_ts, b_ts, c,
+                                             ldc, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k),
+                                             m_tiles2, n_tiles, n_group, static_cast<int>(sfa_rows / 128),
+                                             static_cast<int>(sfb_rows / 128));
+    return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
+}
+
 }  // namespace
 
 h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
                          const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m, int64_t m_pad,
                          int64_t n, int64_t k, const h3fp4_gemm_config &cfg, cudaStream_t st)
 {
-    (void)cfg;
     if (m == 0 || n == 0)
         return H3FP4_OK;
+    if (cfg.cta_pair == 2)
+        return launch_pair(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, st);
     CUtensorMap tmA, tmB;
     if (!make_operand_map(&tmA, a_q, m_pad, k / 2, BM) || !make_operand_map(&tmB, b_q, n, k / 2, BN))
         return H3FP4_ERR_CUDA;

@@ -9,14 +9,15 @@
 // y, compute one E4M3 block scale per 16 values and the E2M1 codes, and write
 // packed QDATA plus the scales directly in the GEMM's 128x4-atom scale layout.
 //
-// Both passes walk the activation in tiles of 128 rows x 256 columns.  A warp
-// reads one 512-byte row segment per instruction (16 bytes per lane), so every
-// load is a full, coalesced 128-byte line set; lanes 2i and 2i+1 hold the two
-// halves of one 16-value block.  A pass-2 tile produces exactly four scale
-// atoms (2 KB, contiguous in the scale layout), which are assembled in shared
-// memory and written with 16-byte stores.  Pass 2 walks the tiles in the
-// reverse of pass 1's order so that its first tiles are the ones pass 1 read
-// last, which are still resident in L2.
+// Both passes walk the activation in tiles of 128 rows x 256 columns.  Each
+// thread owns one 16-value block (32 bytes) of a row, so half a warp covers a
+// 512-byte row segment and every load is coalesced; the block maximum, the
+// E4M3 scale and the reciprocal of the block's scale product are computed
+// once per block, with no cross-lane traffic.  A pass-2 tile produces exactly
+// four scale atoms (2 KB, contiguous in the scale layout), which are assembled
+// in shared memory and written with 16-byte stores.  Pass 2 walks the tiles in
+// the reverse of pass 1's order so that its first tiles are the ones pass 1
+// read last, which are still resident in L2.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -38,8 +39,11 @@ constexpr int kTileRows = 128;
 constexpr int kTileCols = 256;
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowsPerWarp = kTileRows / kWarps;  // 16
-constexpr int kUnroll = 4;                         // rows in flight per lane
+constexpr int kBlock = 16;                          // values per thread and row = one scale block
+constexpr int kRowsPerStep = 2 * kWarps;            // two rows per warp (one per half-warp)
+constexpr int kSteps = kTileRows / kRowsPerStep;    // 8
+constexpr int kUnroll = 2;                          // rows in flight per thread
+constexpr int kMinBlocks = 3;                       // resident CTAs per SM the register budget allows
 
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u)
 {
@@ -90,28 +94,66 @@ __device__ __forceinline__ float e4m3_value(uint32_t c)
     return e ? __uint_as_float(((e + 120u) << 23) | (mant << 20)) : static_cast<float>(mant) * 0.001953125f;
 }
 
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Correctly rounded bf16 silu(g) = g / (1 + e^-g) for one bf16 pattern.
-// FP32 evaluation: expf (at most 2 ulp) then a correctly rounded add and
-// divide leave a relative error below 2^-21, i.e. a few fp32 ulps; when the 16
-// bits below the bf16 rounding point are within 64 of the halfway pattern the
-// rounding is not certain and the table decides.  For g >= -80 the result is a
-// normal fp32 number, so the ulp argument holds.
-__device__ __forceinline__ uint32_t silu_bf16(uint32_t gbits)
+//  - g >= 8: g itself.  g - silu(g) < g e^-g <= 8 e^-8 < 2^-6, which is below
+//    half the bf16 spacing just under g (g >= 8), and shrinks faster than
+//    the spacing grows, so the correctly rounded result is g.
+//  - -16 <= g < 8: FP32 evaluation s = g * rcp(1 + 2^(g * -log2 e)).  The
+//    rounded exponent argument (|argument| <= 23.1) costs at most
+//    0.7 * 23.1 * 2^-23 < 2^-19 relative, the hardware exp2 and reciprocal
+//    approximations about 2^-22 each, the add and multiply 2^-24 each: less
+//    than 2^-18.6 in all, i.e. at most 42 fp32 ulps of s.  When the 16 bits
+//    below the bf16 rounding point are within 128 of the halfway pattern the
+//    rounding is not certain and the build-time table of correctly rounded
+//    values decides; otherwise the bf16 rounding of s is the correct one.
+//  - g < -16 and NaN: the table.
+// Returns the FP32-path result; `unsure` is set when the table must decide.
+__device__ __forceinline__ uint32_t silu_bf16_fast(uint32_t gbits, bool &unsure)
 {
     const float g = __uint_as_float(gbits << 16);
-    if (!(g >= -80.0f))
-        return kSiluLut[gbits];
-    const float e = expf(-g);
-    const float s = __fdiv_rn(g, __fadd_rn(1.0f, e));
+    if (g >= 8.0f) {
+        unsure = false;
+        return gbits;
+    }
+    const float e = ex2_approx(__fmul_rn(g, -0x1.715476p+0f));
+    const float s = __fmul_rn(g, rcp_approx(__fadd_rn(1.0f, e)));
     const uint32_t u = __float_as_uint(s);
-    if ((u & 0xFFFFu) - 0x7FC0u <= 0x80u)
-        return kSiluLut[gbits];
+    unsure = !(g >= -16.0f) || ((u & 0xFFFFu) - 0x7F80u <= 0x100u);
     return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
 }
 
 // ---------------------------------------------------------------------------
 // Sources of the producer values y, 8 consecutive bf16 per lane and row.
 // ---------------------------------------------------------------------------
+struct Vec16 {
+    uint4 lo, hi;
+};
+
+__device__ __forceinline__ Vec16 ld32(const uint16_t *p)
+{
+    return Vec16{ld16(p), ld16(p + 8)};
+}
+
+__device__ __forceinline__ void words(const Vec16 &v, uint32_t (&w)[8])
+{
+    w[0] = v.lo.x; w[1] = v.lo.y; w[2] = v.lo.z; w[3] = v.lo.w;
+    w[4] = v.hi.x; w[5] = v.hi.y; w[6] = v.hi.z; w[7] = v.hi.w;
+}
+
 struct ModulateSrc {
     const uint16_t *x;
     int64_t ldx;
@@ -120,10 +162,10 @@ struct ModulateSrc {
     int64_t ld_mod;
     SegTable seg;
 
-    using Raw = uint4;
+    using Raw = Vec16;
     struct State {
         int64_t begin, end;  // rows of the segment whose parameters are loaded
-        uint32_t s1[4], sh[4];
+        uint32_t s1[8], sh[8];
     };
 
     __device__ __forceinline__ void begin(State &st) const
@@ -131,31 +173,28 @@ struct ModulateSrc {
         st.begin = 1;
         st.end = 0;  // empty range: the first row loads its segment
     }
-    __device__ __forceinline__ Raw load(int64_t r, int col) const { return ld16(x + r * ldx + col); }
+    __device__ __forceinline__ Raw load(int64_t r, int col) const { return ld32(x + r * ldx + col); }
 
     // y = RN_bf16(RN_bf16(x * RN_bf16(scale + 1)) + shift), per segment of row r.
-    __device__ __forceinline__ void apply(State &st, int64_t r, int col, const Raw &raw, uint32_t (&y)[4]) const
+    __device__ __forceinline__ void apply(State &st, int64_t r, int col, const Raw &raw, uint32_t (&y)[8]) const
     {
         if (r < st.begin || r >= st.end) {
             const int s = segment_of(seg, r, st.begin, st.end);
-            const uint4 sc = ld16(scale + s * ld_mod + col);
-            const uint4 sh = ld16(shift + s * ld_mod + col);
+            uint32_t sc[8];
+            words(ld32(scale + s * ld_mod + col), sc);
+            words(ld32(shift + s * ld_mod + col), st.sh);
             const uint32_t one2 = 0x3F803F80u;  // bf16 1.0 in both halves
-            st.s1[0] = bf2_add(sc.x, one2);
-            st.s1[1] = bf2_add(sc.y, one2);
-            st.s1[2] = bf2_add(sc.z, one2);
-            st.s1[3] = bf2_add(sc.w, one2);
-            st.sh[0] = sh.x;
-            st.sh[1] = sh.y;
-            st.sh[2] = sh.z;
-            st.sh[3] = sh.w;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                st.s1[i] = bf2_add(sc[i], one2);
         }
-        y[0] = bf2_add(bf2_mul(raw.x, st.s1[0]), st.sh[0]);
-        y[1] = bf2_add(bf2_mul(raw.y, st.s1[1]), st.sh[1]);
-        y[2] = bf2_add(bf2_mul(raw.z, st.s1[2]), st.sh[2]);
-        y[3] = bf2_add(bf2_mul(raw.w, st.s1[3]), st.sh[3]);
+        uint32_t xw[8];
+        words(raw, xw);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            y[i] = bf2_add(bf2_mul(xw[i], st.s1[i]), st.sh[i]);
     }
-    __device__ __forceinline__ void keep(int64_t, int, const uint32_t (&)[4]) const {}
+    __device__ __forceinline__ void keep(int64_t, int, const uint32_t (&)[8]) const {}
 };
 
 struct SwigluSrc {
@@ -167,31 +206,51 @@ struct SwigluSrc {
     int64_t ldh;
 
     struct Raw {
-        uint4 g, u;
+        Vec16 g, u;
     };
     struct State {};
 
     __device__ __forceinline__ void begin(State &) const {}
     __device__ __forceinline__ Raw load(int64_t r, int col) const
     {
-        return Raw{ld16(g + r * ldg + col), ld16(u + r * ldu + col)};
+        return Raw{ld32(g + r * ldg + col), ld32(u + r * ldu + col)};
     }
 
     // h = RN_bf16(silu_bf16(gate) * up).
-    __device__ __forceinline__ void apply(State &, int64_t, int, const Raw &raw, uint32_t (&y)[4]) const
+    __device__ __forceinline__ void apply(State &, int64_t, int, const Raw &raw, uint32_t (&y)[8]) const
     {
-        const uint32_t gw[4] = {raw.g.x, raw.g.y, raw.g.z, raw.g.w};
-        const uint32_t uw[4] = {raw.u.x, raw.u.y, raw.u.z, raw.u.w};
+        uint32_t gw[8], uw[8], sv[8];
+        words(raw.g, gw);
+        words(raw.u, uw);
+        uint32_t unsure = 0;  // bit 2i / 2i+1: value needs the table
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t s = silu_bf16(gw[i] & 0xFFFFu) | (silu_bf16(gw[i] >> 16) << 16);
-            y[i] = bf2_mul(s, uw[i]);
+        for (int i = 0; i < 8; ++i) {
+            bool ulo, uhi;
+            sv[i] = silu_bf16_fast(gw[i] & 0xFFFFu, ulo) | (silu_bf16_fast(gw[i] >> 16, uhi) << 16);
+            unsure |= (ulo ? 1u : 0u) << (2 * i) | (uhi ? 1u : 0u) << (2 * i + 1);
         }
+        while (unsure) {  // rare: each flagged value is looked up once
+            const int e = __ffs(unsure) - 1;
+            unsure &= unsure - 1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (e == 2 * i)
+                    sv[i] = (sv[i] & 0xFFFF0000u) | kSiluLut[gw[i] & 0xFFFFu];
+                if (e == 2 * i + 1)
+                    sv[i] = (sv[i] & 0x0000FFFFu) | (static_cast<uint32_t>(kSiluLut[gw[i] >> 16]) << 16);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            y[i] = bf2_mul(sv[i], uw[i]);
     }
-    __device__ __forceinline__ void keep(int64_t r, int col, const uint32_t (&y)[4]) const
+    __device__ __forceinline__ void keep(int64_t r, int col, const uint32_t (&y)[8]) const
     {
-        if (h)
-            *reinterpret_cast<uint4 *>(h + r * ldh + col) = make_uint4(y[0], y[1], y[2], y[3]);
+        if (h) {
+            uint4 *dst = reinterpret_cast<uint4 *>(h + r * ldh + col);
+            dst[0] = make_uint4(y[0], y[1], y[2], y[3]);
+            dst[1] = make_uint4(y[4], y[5], y[6], y[7]);
+        }
     }
 };
 
@@ -199,25 +258,29 @@ struct PlainSrc {  // already-materialised bf16 values (SwiGLU pass 2 with a wor
     const uint16_t *h;
     int64_t ldh;
 
-    using Raw = uint4;
+    using Raw = Vec16;
     struct State {};
     __device__ __forceinline__ void begin(State &) const {}
-    __device__ __forceinline__ Raw load(int64_t r, int col) const { return ld16(h + r * ldh + col); }
-    __device__ __forceinline__ void apply(State &, int64_t, int, const Raw &raw, uint32_t (&y)[4]) const
+    __device__ __forceinline__ Raw load(int64_t r, int col) const { return ld32(h + r * ldh + col); }
+    __device__ __forceinline__ void apply(State &, int64_t, int, const Raw &raw, uint32_t (&y)[8]) const
     {
-        y[0] = raw.x;
-        y[1] = raw.y;
-        y[2] = raw.z;
-        y[3] = raw.w;
+        words(raw, y);
     }
-    __device__ __forceinline__ void keep(int64_t, int, const uint32_t (&)[4]) const {}
+    __device__ __forceinline__ void keep(int64_t, int, const uint32_t (&)[8]) const {}
 };
 
-__device__ __forceinline__ uint32_t absmax8(const uint32_t (&y)[4])
+// Bit pattern of max |y| over 16 bf16 values (two per word), with native
+// bf16x2 max on the absolute values; a NaN anywhere gives a NaN pattern
+// (above 0x7F80), which wins every later unsigned comparison.
+__device__ __forceinline__ uint32_t absmax16(const uint32_t (&y)[8])
 {
-    uint32_t v = __vmaxu2(__vmaxu2(y[0] & 0x7FFF7FFFu, y[1] & 0x7FFF7FFFu),
-                          __vmaxu2(y[2] & 0x7FFF7FFFu, y[3] & 0x7FFF7FFFu));
-    return max(v & 0xFFFFu, v >> 16);
+    __nv_bfloat162 v = as_bf2(y[0] & 0x7FFF7FFFu);
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+        v = __hmax2_nan(v, as_bf2(y[i] & 0x7FFF7FFFu));
+    const uint32_t w = as_u32(v);
+    const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+    return max(lo, hi);   // both non-negative patterns: integer order = value order, NaN above all
 }
 
 // ---------------------------------------------------------------------------
@@ -226,33 +289,34 @@ __device__ __forceinline__ uint32_t absmax8(const uint32_t (&y)[4])
 // (counted in scratch[1]) converts the maximum into the tensor scale.
 // ---------------------------------------------------------------------------
 template <class Src>
-__global__ void __launch_bounds__(kThreads) absmax_kernel(Src src, int64_t m, int col_tiles, int64_t n_tiles,
+__global__ void __launch_bounds__(kThreads, kMinBlocks) absmax_kernel(Src src, int64_t m, int col_tiles, int64_t n_tiles,
                                                           uint32_t *scratch, float *ts_out)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane & 15, half = lane >> 4;
     typename Src::State st;
     uint32_t vmax = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         const int64_t row0 = (t / col_tiles) * kTileRows;
-        const int col = static_cast<int>(t % col_tiles) * kTileCols + lane * 8;
+        const int col = static_cast<int>(t % col_tiles) * kTileCols + sub * kBlock;
         src.begin(st);  // cached per-column parameters belong to the previous tile's columns
 #pragma unroll 1
-        for (int i0 = 0; i0 < kRowsPerWarp; i0 += kUnroll) {
+        for (int i0 = 0; i0 < kSteps; i0 += kUnroll) {
             typename Src::Raw raw[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                const int64_t r = row0 + warp + kWarps * (i0 + u);
+                const int64_t r = row0 + kRowsPerStep * (i0 + u) + 2 * warp + half;
                 if (r < m)
                     raw[u] = src.load(r, col);
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                const int64_t r = row0 + warp + kWarps * (i0 + u);
+                const int64_t r = row0 + kRowsPerStep * (i0 + u) + 2 * warp + half;
                 if (r < m) {
-                    uint32_t y[4];
+                    uint32_t y[8];
                     src.apply(st, r, col, raw[u], y);
                     src.keep(r, col, y);
-                    vmax = max(vmax, absmax8(y));
+                    vmax = max(vmax, absmax16(y));
                 }
             }
         }
@@ -279,110 +343,136 @@ __global__ void __launch_bounds__(kThreads) absmax_kernel(Src src, int64_t m, in
     }
 }
 
-// True when q (>= 0) lies within 32 fp32 ulps of a number with at most three
-// significant bits.  Every E2M1 rounding midpoint (0.25, 0.75, 1.25, 1.75,
-// 2.5, 3.5, 5) is such a number.
-__device__ __forceinline__ bool near_short_value(float q)
+// Bits 6..20 of (u + 32) are all zero exactly when the low 21 bits of u lie in
+// [2^21 - 32, 2^21) or [0, 32), i.e. when the fp32 value with bits u lies
+// within 32 ulps of a number with at most three significant bits (the sign is
+// ignored).  Every E2M1 rounding midpoint (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5)
+// is such a number.
+constexpr uint32_t kShort3Mask = 0x1FFFC0u;
+// The same with the low 19 bits, for five significant bits: every E4M3
+// rounding boundary (normal midpoints 1.mmm1 x 2^e, subnormal midpoints
+// (2j+1) x 2^-10) is such a number.
+constexpr uint32_t kShort5Mask = 0x7FFC0u;
+
+// Block scale bs = E4M3_RNE_sat(RN_f32(bamax / den)) from rden = RN(1/den):
+// q = RN(bamax * rden) is within 2^-22 (relative) of the exact quotient, so
+// the E4M3 rounding of q and of RN_f32(bamax / den) can only differ when q is
+// within a few ulps of a boundary; those, and dens whose reciprocal is not a
+// normal number, take the IEEE division.
+__device__ __forceinline__ uint32_t block_scale(uint32_t bmax_bits, float den, float rden, bool den_normal)
 {
-    return ((__float_as_uint(q) + 32u) & 0x1FFFFFu) < 64u;
+    if (bmax_bits == 0)
+        return 0u;  // an all-zero block gets scale 0
+    const float b = __uint_as_float(bmax_bits << 16);
+    float q = __fmul_rn(b, rden);
+    if (!den_normal || ((__float_as_uint(q) + 32u) & kShort5Mask) == 0u)
+        q = __fdiv_rn(b, den);
+    return cvt_e4m3(q);
 }
 
-// E2M1 codes of 8 values with the block's FP32 scale product sc; byte i holds
-// element 2i in its low nibble.  A zero scale product gives signed zeros.
+// E2M1 codes of a 16-value block with the block's FP32 scale product sc;
+// byte i holds element 2i in its low nibble.  A zero scale product gives
+// signed zeros.
 //
-// The code of y is E2M1_RNE_sat(RN_f32(y / sc)); the sign is taken from y and
-// the magnitude rounded from |y|.  Instead of one IEEE division per value the
-// block computes r = RN(1/sc) once and q = RN(|y| * r), which differs from the
-// exact quotient by less than 2^-22 (relative).  The E2M1 rounding of q and of
-// RN_f32(|y| / sc) can only differ when a midpoint lies within that distance,
-// i.e. when q is within 8 ulps of a midpoint; any q within 32 ulps of a
-// three-significant-bit number is recomputed with the IEEE division.  Scale
-// products outside [2^-125, 2^125], whose reciprocal is not a normal number,
-// always take the division.
-__device__ __forceinline__ uint32_t encode8(const uint32_t (&y)[4], float sc)
+// The code of y is E2M1_RNE_sat(RN_f32(y / sc)).  Instead of one IEEE division
+// per value the block computes r = RN(1/sc) once and q = RN(y * r), which
+// differs from the exact quotient by less than 2^-22 (relative).  The E2M1
+// rounding of q and of RN_f32(y / sc) can only differ when a midpoint lies
+// within that distance, i.e. when |q| is within 8 ulps of a midpoint; if any
+// value of a half block is within 32 ulps of a three-significant-bit number,
+// that half is recomputed with the IEEE division.  Scale products outside
+// [2^-125, 2^125], whose reciprocal is not a normal number, always take the
+// division.  Quotients keep y's sign (also for y = -0), and the conversion
+// keeps the sign of zero, so a negative value that rounds to 0 gives 0x8.
+__device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
 {
-    uint32_t signs = 0;
+    if (sc == 0.0f) {
+        uint32_t signs[2] = {0u, 0u};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        signs |= (((y[i] >> 12) & 0x8u) | ((y[i] >> 24) & 0x80u)) << (8 * i);
-    if (sc == 0.0f)
-        return signs;
-    float a[8], q[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        a[2 * i] = __uint_as_float((y[i] & 0x7FFFu) << 16);
-        a[2 * i + 1] = __uint_as_float(y[i] & 0x7FFF0000u);
+        for (int i = 0; i < 8; ++i)
+            signs[i >> 2] |= (((y[i] >> 12) & 0x8u) | ((y[i] >> 24) & 0x80u)) << (8 * (i & 3));
+        return make_uint2(signs[0], signs[1]);
     }
-    bool slow = !(sc >= 0x1p-125f && sc <= 0x1p125f);
-    if (!slow) {
-        const float r = __frcp_rn(sc);
+    const bool normal_range = sc >= 0x1p-125f && sc <= 0x1p125f;
+    const float r = normal_range ? __frcp_rn(sc) : 0.0f;
+    uint32_t out[2];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            q[e] = __fmul_rn(a[e], r);
-            slow |= near_short_value(q[e]);
+    for (int hlf = 0; hlf < 2; ++hlf) {   // 8 values (4 words) at a time keeps fewer registers live
+        float a[8], q[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            a[2 * i] = __uint_as_float(y[4 * hlf + i] << 16);
+            a[2 * i + 1] = __uint_as_float(y[4 * hlf + i] & 0xFFFF0000u);
         }
-    }
-    if (slow) {
+        bool slow = !normal_range;
+        if (!slow) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            q[e] = __fdiv_rn(a[e], sc);
-    }
-    uint32_t out = 0;
+            for (int e = 0; e < 8; ++e) {
+                q[e] = __fmul_rn(a[e], r);
+                slow |= ((__float_as_uint(q[e]) + 32u) & kShort3Mask) == 0u;
+            }
+        }
+        if (slow) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        out |= cvt_e2m1x2(q[2 * i + 1], q[2 * i]) << (8 * i);
-    return out | signs;
+            for (int e = 0; e < 8; ++e)
+                q[e] = __fdiv_rn(a[e], sc);
+        }
+        uint32_t o = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o |= cvt_e2m1x2(q[2 * i + 1], q[2 * i]) << (8 * i);
+        out[hlf] = o;
+    }
+    return make_uint2(out[0], out[1]);
 }
 
 // ---------------------------------------------------------------------------
 // Pass 2: one CTA per 128 x 256 tile (tiles visited in reverse order).
 // ---------------------------------------------------------------------------
 template <class Src>
-__global__ void __launch_bounds__(kThreads) pack_kernel(Src src, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
+__global__ void __launch_bounds__(kThreads, kMinBlocks) pack_kernel(Src src, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
                                                         int64_t n_tiles, const float *ts_ptr, uint8_t *qdata,
                                                         uint8_t *sf)
 {
     __shared__ __align__(16) uint8_t sft[4 * 512];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane & 15, half = lane >> 4;
     const int64_t t = n_tiles - 1 - blockIdx.x;
     const int64_t row_tile = t / col_tiles;
     const int col_tile = static_cast<int>(t % col_tiles);
     const int64_t row0 = row_tile * kTileRows;
-    const int col = col_tile * kTileCols + lane * 8;
+    const int col = col_tile * kTileCols + sub * kBlock;
     const int64_t qld = d / 2;
     const float ts = *ts_ptr;
     const float den = __fmul_rn(6.0f, ts);
+    const bool den_normal = den >= 0x1p-125f && den <= 0x1p125f;
+    const float rden = den_normal ? __frcp_rn(den) : 0.0f;
     typename Src::State st;
     src.begin(st);
 
 #pragma unroll 1
-    for (int i0 = 0; i0 < kRowsPerWarp; i0 += kUnroll) {
+    for (int i0 = 0; i0 < kSteps; i0 += kUnroll) {
         typename Src::Raw raw[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int64_t r = row0 + warp + kWarps * (i0 + u);
+            const int64_t r = row0 + kRowsPerStep * (i0 + u) + 2 * warp + half;
             if (r < m)
                 raw[u] = src.load(r, col);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int rr = warp + kWarps * (i0 + u);
+            const int rr = kRowsPerStep * (i0 + u) + 2 * warp + half;
             const int64_t r = row0 + rr;
-            uint32_t y[4] = {0u, 0u, 0u, 0u};
+            uint32_t y[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
             if (r < m)
                 src.apply(st, r, col, raw[u], y);
-            const uint32_t a = absmax8(y);
-            const uint32_t bmax = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
             // bs = E4M3_RNE_sat(RN_f32(block_amax / RN_f32(6 ts))); an all-zero block gets 0.
-            const uint32_t bs = bmax ? cvt_e4m3(__fdiv_rn(__uint_as_float(bmax << 16), den)) : 0u;
+            const uint32_t bs = block_scale(absmax16(y), den, rden, den_normal);
             const float sc = __fmul_rn(e4m3_value(bs), ts);
-            const uint32_t packed = encode8(y, sc);
+            const uint2 packed = encode16(y, sc);
             if (r < m_pad)
-                *reinterpret_cast<uint32_t *>(qdata + r * qld + col / 2) = packed;
-            if ((lane & 1) == 0) {
-                const int b = lane >> 1;  // block within the tile, 0..15
-                sft[(b >> 2) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (b & 3)] = static_cast<uint8_t>(bs);
-            }
+                *reinterpret_cast<uint2 *>(qdata + r * qld + col / 2) = packed;
+            sft[(sub >> 2) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (sub & 3)] = static_cast<uint8_t>(bs);
         }
     }
     __syncthreads();

@@ -28,6 +28,8 @@ def main():
     ap.add_argument("--n", type=int, default=21504)
     ap.add_argument("--k", type=int, default=7168)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--cta-pair", type=int, default=0, help="GEMM kernel: 0 default, 1 single CTA, 2 CTA pairs")
+    ap.add_argument("--n-group", type=int, default=0, help="GEMM N-group (0 = default)")
     a = ap.parse_args()
     B.build()
     dev = torch.device("cuda")
@@ -55,9 +57,10 @@ def main():
             bsf = h3.swizzle_scales(wt["sf"][: a.n])
             bts = torch.tensor([wt["ts"]], dtype=torch.float32, device=dev)
             c = torch.empty(a.m, a.n, dtype=torch.int16, device=dev)
+            cfg = h3.GemmConfig(a.n_group, 0, a.cta_pair, 0)
 
             def call():
-                h3.gemm(q, sfa, ts, wt["q"], bsf, bts, a.m, out=c)
+                h3.gemm(q, sfa, ts, wt["q"], bsf, bts, a.m, out=c, cfg=cfg)
     for _ in range(2):
         call()
     torch.cuda.synchronize()
@@ -70,7 +73,8 @@ def main():
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
     assert h3.h3fp4_device_error() == 0
-    print(f"{a.op} m={a.m} n={a.n} k={a.k}: {e0.elapsed_time(e1) / a.reps:.4f} ms per call")
+    extra = f" cta_pair={a.cta_pair} n_group={a.n_group}" if a.op == "gemm" else ""
+    print(f"{a.op} m={a.m} n={a.n} k={a.k}{extra}: {e0.elapsed_time(e1) / a.reps:.4f} ms per call")
 
 
 if __name__ == "__main__":

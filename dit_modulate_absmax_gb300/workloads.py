@@ -101,6 +101,8 @@ def activations(w: Workload, device="cpu", m: int | None = None) -> dict:
 def seg_offsets(w: Workload, m: int | None = None) -> list:
     """Segment row offsets, with the last one clipped to m rows."""
     m = w.m if m is None else m
+    if not w.seg_off:
+        return [0, m]
     offs = [min(o, m) for o in w.seg_off]
     offs[-1] = m
     return offs

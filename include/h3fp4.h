@@ -142,11 +142,14 @@ typedef struct h3fp4_gemm_config {
     /* N-group A-tile reuse factor: the persistent schedule walks the 128 x 256
      * output tiles in groups of n_group N-tiles x all M-tiles, N fastest, so
      * each 128-row A tile serves n_group consecutive output tiles while it is
-     * L2-resident (0 = default 16; values above the number of N-tiles are
+     * L2-resident (0 = default 28; values above the number of N-tiles are
      * clamped). */
     int32_t n_group;
-    int32_t stages;    /* reserved, must be 0 (the pipeline depth is fixed at 4) */
-    int32_t cta_pair;  /* reserved, must be 0 */
+    int32_t stages;    /* reserved, must be 0 (the pipeline depth is fixed per kernel) */
+    /* GEMM kernel: 0 = library default, 1 = one CTA per 128 x 256 output tile
+     * (4-stage ring), 2 = CTA pairs on two SMs per 256 x 256 tile (tcgen05
+     * cta_group::2, each SM loads half of A and half of B; 5-stage ring). */
+    int32_t cta_pair;
     int32_t reserved;  /* must be 0 */
 } h3fp4_gemm_config;
 

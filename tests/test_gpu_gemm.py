@@ -16,6 +16,15 @@ from dit_modulate_absmax_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 CANARY16 = 0x7E7E
 
+# Both GEMM kernels: one CTA per 128 x 256 tile (cta_pair=1) and CTA pairs on
+# 256 x 256 tiles (cta_pair=2).
+KERNELS = {"single": 1, "pair": 2}
+
+
+@pytest.fixture(params=sorted(KERNELS), ids=sorted(KERNELS))
+def cfg(request, h3):
+    return h3.GemmConfig(0, 0, KERNELS[request.param], 0)
+
 
 def _rand_operand(rng, rows, k, code_lo, code_hi, sf_rows=None):
     q = rng.integers(0, 256, size=(rows, k // 2), dtype=np.uint8)
@@ -25,7 +34,7 @@ def _rand_operand(rng, rows, k, code_lo, code_hi, sf_rows=None):
     return q, sf
 
 
-def run_gemm(h3, qa, sfa, ts_a, qb, sfb, ts_b, m, ldc=None, extra_rows=3):
+def run_gemm(h3, qa, sfa, ts_a, qb, sfb, ts_b, m, ldc=None, extra_rows=3, cfg=None):
     m_pad, kh = qa.shape
     n = qb.shape[0]
     ldc = n if ldc is None else ldc
@@ -36,7 +45,7 @@ def run_gemm(h3, qa, sfa, ts_a, qb, sfb, ts_b, m, ldc=None, extra_rows=3):
     ta = torch.tensor([ts_a], dtype=torch.float32, device="cuda")
     tb = torch.tensor([ts_b], dtype=torch.float32, device="cuda")
     cbuf = torch.full((m + extra_rows, ldc), CANARY16, dtype=torch.int16, device="cuda")
-    h3.gemm(a_q, a_sf, ta, b_q, b_sf, tb, m, out=cbuf[:m].as_strided((m, n), (ldc, 1)))
+    h3.gemm(a_q, a_sf, ta, b_q, b_sf, tb, m, out=cbuf[:m].as_strided((m, n), (ldc, 1)), cfg=cfg)
     torch.cuda.synchronize()
     assert h3.h3fp4_device_error() == 0
     c = cbuf.cpu().numpy().view(np.uint16)
@@ -53,7 +62,7 @@ def check_tolerance(C, R, S):
     return err / tol
 
 
-def test_exact_products_are_bit_exact(h3):
+def test_exact_products_are_bit_exact(h3, cfg):
     """Power-of-two scales: every product and partial sum is exact, so C = RN_bf16(R)."""
     rng = np.random.default_rng(20)
     m, m_pad, n, k = 200, 256, 384, 512
@@ -68,7 +77,7 @@ def test_exact_products_are_bit_exact(h3):
     sfa[:m] = rng.choice(pow2, size=(m, k // 16))
     sfb[:n] = rng.choice(pow2, size=(n, k // 16))
     ts_a, ts_b = 0.125, 4.0                                               # alpha = 0.5
-    C = run_gemm(h3, qa, sfa, ts_a, qb, sfb, ts_b, m)
+    C = run_gemm(h3, qa, sfa, ts_a, qb, sfb, ts_b, m, cfg=cfg)
     R, S = oracle.gemm_reference(qa, sfa, ts_a, qb, sfb, ts_b, k, rows=np.arange(m))
     want = np.vectorize(oracle.bf16_bits)(R).astype(np.uint16)
     bad = np.argwhere(C != want)
@@ -82,28 +91,28 @@ def test_exact_products_are_bit_exact(h3):
     (513, 528, 640, 1024),
     (128, 128, 512, 2048),
 ])
-def test_random_shapes_within_tolerance(h3, m, m_pad, n, k):
+def test_random_shapes_within_tolerance(h3, cfg, m, m_pad, n, k):
     rng = np.random.default_rng(m * 7 + n + k)
     qa, sfa = _rand_operand(rng, m_pad, k, 0x28, 0x50)
     qa[m:] = 0
     sfa[m:] = 0
     qb, sfb = _rand_operand(rng, n, k, 0x28, 0x50)
-    C = run_gemm(h3, qa, sfa, 0.0123, qb, sfb, 2.0 ** -10, m)
+    C = run_gemm(h3, qa, sfa, 0.0123, qb, sfb, 2.0 ** -10, m, cfg=cfg)
     R, S = oracle.gemm_reference(qa, sfa, 0.0123, qb, sfb, 2.0 ** -10, k, rows=np.arange(m))
     check_tolerance(C, R, S)
 
 
-def test_leading_dimension_of_c(h3):
+def test_leading_dimension_of_c(h3, cfg):
     rng = np.random.default_rng(22)
     m, m_pad, n, k, ldc = 100, 112, 256, 512, 264
     qa, sfa = _rand_operand(rng, m_pad, k, 0x30, 0x48)
     qb, sfb = _rand_operand(rng, n, k, 0x30, 0x48)
-    C = run_gemm(h3, qa, sfa, 1.0, qb, sfb, 1.0, m, ldc=ldc)
+    C = run_gemm(h3, qa, sfa, 1.0, qb, sfb, 1.0, m, ldc=ldc, cfg=cfg)
     R, S = oracle.gemm_reference(qa, sfa, 1.0, qb, sfb, 1.0, k, rows=np.arange(m))
     check_tolerance(C, R, S)
 
 
-def test_tiny_workload_end_to_end(h3):
+def test_tiny_workload_end_to_end(h3, cfg):
     """Adversarial tiny producer on the GPU, then the GEMM, against the oracle's whole chain."""
     from oracle.adversarial import tiny_adversarial
     w = W.WORKLOADS["tiny"]
@@ -121,21 +130,21 @@ def test_tiny_workload_end_to_end(h3):
     bq = wt["q"].cuda()
     bsf = h3.swizzle_scales(wt["sf"][: w.n].cuda())
     bts = torch.tensor([wt["ts"]], dtype=torch.float32, device="cuda")
-    C = h3.gemm(q, sfa, ts, bq, bsf, bts, w.m)
+    C = h3.gemm(q, sfa, ts, bq, bsf, bts, w.m, cfg=cfg)
     torch.cuda.synchronize()
     R, S = oracle.gemm_reference(q_o, sf_o, ts_o, wt["q"].numpy(), wt["sf"].numpy(), wt["ts"], w.k,
                                  rows=np.arange(w.m))
     check_tolerance(C.cpu().numpy().view(np.uint16), R, S)
 
 
-def test_zero_rows_writes_nothing(h3):
+def test_zero_rows_writes_nothing(h3, cfg):
     rng = np.random.default_rng(23)
     qa, sfa = _rand_operand(rng, 16, 256, 0x30, 0x40)
     qb, sfb = _rand_operand(rng, 128, 256, 0x30, 0x40)
-    run_gemm(h3, qa, sfa, 1.0, qb, sfb, 1.0, 0, extra_rows=4)
+    run_gemm(h3, qa, sfa, 1.0, qb, sfb, 1.0, 0, extra_rows=4, cfg=cfg)
 
 
-def test_scale_atom_rows_are_not_mixed(h3):
+def test_scale_atom_rows_are_not_mixed(h3, cfg):
     """Rows i and columns j get only their own scales: one nonzero scale row per operand."""
     rng = np.random.default_rng(24)
     m, m_pad, n, k = 256, 256, 256, 512
@@ -147,7 +156,7 @@ def test_scale_atom_rows_are_not_mixed(h3):
         sfa[r] = 0x38
     for c in (1, 64, 127, 128, 200):
         sfb[c, 3] = 0x40            # only scale column 3 (K elements 48..63) of these rows
-    C = run_gemm(h3, qa, sfa, 1.0, qb, sfb, 1.0, m)
+    C = run_gemm(h3, qa, sfa, 1.0, qb, sfb, 1.0, m, cfg=cfg)
     R, S = oracle.gemm_reference(qa, sfa, 1.0, qb, sfb, 1.0, k, rows=np.arange(m))
     nz = np.argwhere(R != 0)
     assert set(map(int, np.unique(nz[:, 0]))) <= {0, 37, 95, 130, 255}

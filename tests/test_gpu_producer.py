@@ -103,6 +103,14 @@ def test_ctas_walking_several_tiles_bit_exact(h3):
     check_modulate(h3, x, sh, sc, [0, 9000, m], m + 3)
 
 
+def test_many_blocks_bit_exact(h3):
+    """16.8 M values: enough quotients land within a few ulps of an E2M1 or E4M3
+    rounding boundary to exercise both sides of the reciprocal fast path."""
+    m, d = 8192, 2048
+    x, sh, sc = _random_case(m, d, 2, seed=19, scale=3.0)
+    check_modulate(h3, x, sh, sc, [0, 5000, m], m)
+
+
 def test_many_segments_bit_exact(h3):
     m, d = 700, 256
     off = list(range(0, 700, 50)) + [700]          # 14 segments of 50 rows
