@@ -116,11 +116,12 @@ __device__ __forceinline__ float rcp_approx(float x)
 //    rounded exponent argument (|argument| <= 23.1) costs at most
 //    0.7 * 23.1 * 2^-23 < 2^-19 relative, the hardware exp2 and reciprocal
 //    approximations about 2^-22 each, the add and multiply 2^-24 each: less
-//    than 2^-18.6 in all, i.e. at most 42 fp32 ulps of s.  When the 16 bits
-//    below the bf16 rounding point are within 128 of the halfway pattern the
-//    rounding is not certain and the build-time table of correctly rounded
-//    values decides; otherwise the bf16 rounding of s is the correct one.
-//  - g < -16 and NaN: the table.
+//    than 2^-18.6 in all.  So the exact silu lies between s (1 - 2^-17) and
+//    s (1 + 2^-17); bf16 rounding is monotone, so when both round to the same
+//    bf16 value that value is the correctly rounded silu.  Otherwise (a bf16
+//    rounding boundary within 2^-17 of s) the build-time table decides.
+//  - g < -16, |g| < 2^-100 (where s (1 +- 2^-17) can underflow to the same
+//    subnormal and the sandwich collapses) and NaN: the table.
 // Returns the FP32-path result; `unsure` is set when the table must decide.
 __device__ __forceinline__ uint32_t silu_bf16_fast(uint32_t gbits, bool &unsure)
 {
@@ -131,9 +132,11 @@ __device__ __forceinline__ uint32_t silu_bf16_fast(uint32_t gbits, bool &unsure)
     }
     const float e = ex2_approx(__fmul_rn(g, -0x1.715476p+0f));
     const float s = __fmul_rn(g, rcp_approx(__fadd_rn(1.0f, e)));
-    const uint32_t u = __float_as_uint(s);
-    unsure = !(g >= -16.0f) || ((u & 0xFFFFu) - 0x7F80u <= 0x100u);
-    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+    const __nv_bfloat162 both = __floats2bfloat162_rn(__fmul_rn(s, 1.0f - 0x1p-17f), __fmul_rn(s, 1.0f + 0x1p-17f));
+    uint32_t u;
+    memcpy(&u, &both, 4);
+    unsure = !(g >= -16.0f) || !(fabsf(g) >= 0x1p-100f) || ((u ^ (u >> 16)) & 0xFFFFu) != 0u;
+    return u & 0xFFFFu;
 }
 
 // ---------------------------------------------------------------------------
@@ -343,13 +346,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) absmax_kernel(Src src, i
     }
 }
 
-// Bits 6..20 of (u + 32) are all zero exactly when the low 21 bits of u lie in
-// [2^21 - 32, 2^21) or [0, 32), i.e. when the fp32 value with bits u lies
-// within 32 ulps of a number with at most three significant bits (the sign is
-// ignored).  Every E2M1 rounding midpoint (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5)
-// is such a number.
-constexpr uint32_t kShort3Mask = 0x1FFFC0u;
-// The same with the low 19 bits, for five significant bits: every E4M3
+// Bits 6..18 of (u + 32) are all zero exactly when the low 19 bits of u lie
+// in [2^19 - 32, 2^19) or [0, 32), i.e. when the fp32 value with bits u lies
+// within 32 ulps of a number with at most five significant bits (the sign is
+// ignored).  Every E4M3
 // rounding boundary (normal midpoints 1.mmm1 x 2^e, subnormal midpoints
 // (2j+1) x 2^-10) is such a number.
 constexpr uint32_t kShort5Mask = 0x7FFC0u;
@@ -375,15 +375,18 @@ __device__ __forceinline__ uint32_t block_scale(uint32_t bmax_bits, float den, f
 // signed zeros.
 //
 // The code of y is E2M1_RNE_sat(RN_f32(y / sc)).  Instead of one IEEE division
-// per value the block computes r = RN(1/sc) once and q = RN(y * r), which
-// differs from the exact quotient by less than 2^-22 (relative).  The E2M1
-// rounding of q and of RN_f32(y / sc) can only differ when a midpoint lies
-// within that distance, i.e. when |q| is within 8 ulps of a midpoint; if any
-// value of a half block is within 32 ulps of a three-significant-bit number,
-// that half is recomputed with the IEEE division.  Scale products outside
-// [2^-125, 2^125], whose reciprocal is not a normal number, always take the
-// division.  Quotients keep y's sign (also for y = -0), and the conversion
-// keeps the sign of zero, so a negative value that rounds to 0 gives 0x8.
+// per value the block computes r = RN(1/sc) and two nudged reciprocals
+// r_lo = RN(r (1 - 2^-20)), r_hi = RN(r (1 + 2^-20)), and each value is
+// converted twice, from q_lo = RN(y r_lo) and q_hi = RN(y r_hi).  With
+// v = y/sc exact and sc, 1/sc normal, |y r - v| <= 2^-23 |v| up to rounding,
+// so |q_lo| < |v| (1 - 2^-21) < |RN_f32(v)| and |q_hi| > |RN_f32(v)|: the
+// correctly rounded quotient lies between q_lo and q_hi.  Rounding to E2M1 is
+// monotone, so where both conversions agree they give the code of
+// RN_f32(v) (quotients below the normal range round to a signed zero either
+// way).  Where they differ -- some rounding boundary lies within 2^-20 of the
+// quotient, a rare case -- those 8 values are redone with the IEEE division;
+// so are whole blocks whose sc lies outside [2^-125, 2^125].  The sign of y
+// (also of y = -0) carries through the products into the code.
 __device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
 {
     if (sc == 0.0f) {
@@ -395,33 +398,31 @@ __device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
     }
     const bool normal_range = sc >= 0x1p-125f && sc <= 0x1p125f;
     const float r = normal_range ? __frcp_rn(sc) : 0.0f;
+    const float r_lo = __fmul_rn(r, 1.0f - 0x1p-20f);
+    const float r_hi = __fmul_rn(r, 1.0f + 0x1p-20f);
     uint32_t out[2];
 #pragma unroll
-    for (int hlf = 0; hlf < 2; ++hlf) {   // 8 values (4 words) at a time keeps fewer registers live
-        float a[8], q[8];
+    for (int hlf = 0; hlf < 2; ++hlf) {   // 8 values (4 words) at a time
+        uint32_t lo = 0, diff = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            a[2 * i] = __uint_as_float(y[4 * hlf + i] << 16);
-            a[2 * i + 1] = __uint_as_float(y[4 * hlf + i] & 0xFFFF0000u);
+            const uint32_t w = y[4 * hlf + i];
+            const float a0 = __uint_as_float(w << 16), a1 = __uint_as_float(w & 0xFFFF0000u);
+            const uint32_t b_lo = cvt_e2m1x2(__fmul_rn(a1, r_lo), __fmul_rn(a0, r_lo));
+            const uint32_t b_hi = cvt_e2m1x2(__fmul_rn(a1, r_hi), __fmul_rn(a0, r_hi));
+            diff |= b_lo ^ b_hi;
+            lo |= b_lo << (8 * i);
         }
-        bool slow = !normal_range;
-        if (!slow) {
+        if (!normal_range || diff != 0u) {   // rare: redo these 8 values with the IEEE division
+            lo = 0;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                q[e] = __fmul_rn(a[e], r);
-                slow |= ((__float_as_uint(q[e]) + 32u) & kShort3Mask) == 0u;
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w = y[4 * hlf + i];
+                lo |= cvt_e2m1x2(__fdiv_rn(__uint_as_float(w & 0xFFFF0000u), sc), __fdiv_rn(__uint_as_float(w << 16), sc))
+                      << (8 * i);
             }
         }
-        if (slow) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                q[e] = __fdiv_rn(a[e], sc);
-        }
-        uint32_t o = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            o |= cvt_e2m1x2(q[2 * i + 1], q[2 * i]) << (8 * i);
-        out[hlf] = o;
+        out[hlf] = lo;
     }
     return make_uint2(out[0], out[1]);
 }
