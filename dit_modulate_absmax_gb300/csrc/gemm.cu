@@ -23,9 +23,13 @@
 //               the atoms with tcgen05.cp instead costs twelve tensor-pipe
 //               instructions per stage, which measured as the main limiter.)
 //   warps 2-9   epilogue: each warp drains one 32-lane quarter x 128 columns of
-//               the accumulator into registers (tcgen05.ld), releases the
-//               accumulator at once so that the next tile's MMAs can start, and
-//               then applies alpha, converts to bf16 and stores.
+//               the accumulator into registers (tcgen05.ld), applying alpha and
+//               converting to bf16 as it goes, releases the accumulator at once
+//               so that the next tile's MMAs can start, and then writes its 32 x
+//               128 block with 16-column TMA tensor stores staged through a 1 KB
+//               shared-memory buffer of its own (per-lane stores from the
+//               row-per-lane accumulator layout would touch 32 rows per
+//               instruction; they measured 18% slower end to end).
 // Tiles (128 x 256 outputs) are visited in groups of n_group N-tiles x all
 // M-tiles with N fastest, so every 128-row A tile is used by n_group
 // consecutive tiles while it is L2-resident, and the B tiles of a group stay
@@ -73,6 +77,8 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SF_COL = 256;
 constexpr uint32_t SF_COLS_PER_STAGE = 48;  // 16 for A, 32 for B
+constexpr int CST_COLS = 16;                // output columns per tensor store (32 rows x 32 bytes)
+constexpr uint32_t CST_BYTES = 32 * CST_COLS * 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Device error codes (OR-ed into g_device_error).
@@ -87,6 +93,7 @@ struct __align__(1024) Smem {
     uint8_t b[kStages][B_BYTES];
     uint8_t sfa[kStages][SFA_BYTES];
     uint8_t sfb[kStages][SFB_BYTES];
+    uint8_t cst[kEpiWarps][CST_BYTES];  // per epilogue warp: output staging for tensor stores
     uint64_t full[kStages];      // A and B tiles landed
     uint64_t sf_full[kStages];   // scale atoms landed
     uint64_t empty[kStages];
@@ -114,18 +121,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// Moves one stage's scale atoms from shared memory into TMEM, in the layout
-// the block-scaled MMA reads: for MMA K step j, row i (16 bytes) of the
-// 128x4 atom goes to columns 4j .. 4j+3 of lane 32q + i for every lane
-// quarter q, i.e. the layout of a tcgen05.cp .32x128b.warpx4 copy of the atom.
-// SFA (4 atoms, one per K step) lands at sfa_col (16 columns); SFB (two
-// 128-row halves x 4 atoms) at sfb_col (32 columns: step j, half h at 8j + 4h).
-// Executed by a whole warp; `lane_base` selects the warp's lane quarter.
-// One tcgen05.st per operand replaces twelve tcgen05.cp in the tensor pipe.
-__device__ __forceinline__ void stage_scales(uint32_t lane_base, uint32_t sfa_col, uint32_t sfb_col,
-                                             const uint8_t *sfa, const uint8_t *sfb, int lane)
+// The scale layout the block-scaled MMA reads from TMEM: for MMA K step j,
+// row i (16 bytes) of the 128x4 atom goes to columns 4j .. 4j+3 of lane
+// 32q + i for every lane quarter q, i.e. the layout of a tcgen05.cp
+// .32x128b.warpx4 copy of the atom.  SFA (4 atoms, one per K step) takes 16
+// columns; SFB (two 128-row halves x 4 atoms) takes 32 columns, step j and
+// half h at 8j + 4h.  read_scales gathers, for one lane, the words it writes:
+// a[] for SFA, b[] for SFB.
+__device__ __forceinline__ void read_scales(const uint8_t *sfa, const uint8_t *sfb, int lane, uint32_t (&a)[16],
+                                            uint32_t (&b)[32])
 {
-    uint32_t a[16], b[32];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint4 v = *reinterpret_cast<const uint4 *>(sfa + j * ATOM + lane * 16);
@@ -144,9 +149,46 @@ __device__ __forceinline__ void stage_scales(uint32_t lane_base, uint32_t sfa_co
             b[8 * j + 4 * h + 2] = v.z;
             b[8 * j + 4 * h + 3] = v.w;
         }
+}
+
+// Moves one stage's scale atoms from shared memory into TMEM (SFA at sfa_col,
+// SFB at sfb_col).  Executed by a whole warp; `lane_base` selects the warp's
+// lane quarter.  One tcgen05.st per operand replaces twelve tcgen05.cp in the
+// tensor pipe.
+__device__ __forceinline__ void stage_scales(uint32_t lane_base, uint32_t sfa_col, uint32_t sfb_col,
+                                             const uint8_t *sfa, const uint8_t *sfb, int lane)
+{
+    uint32_t a[16], b[32];
+    read_scales(sfa, sfb, lane, a, b);
     tmem_st_32x32b_x16(lane_base + sfa_col, a);
     tmem_st_32x32b_x32(lane_base + sfb_col, b);
     tmem_st_wait();
+}
+
+// Writes one epilogue warp's 32 output rows x 128 bf16 columns (row = lane;
+// pk[i] holds columns 2i and 2i+1) with 16-column tensor stores through the
+// warp's 1 KB shared-memory buffer.  The per-lane global stores this replaces
+// wrote 16 bytes into each of 32 different rows per instruction; a tensor
+// store moves whole 32-byte row pieces of the 32 x 16 block.  Rows at or past
+// the tensor map's M extent (the padding of the last M tile) are not written.
+__device__ __forceinline__ void store_rows(const CUtensorMap *tmC, uint32_t buf, const uint32_t (&pk)[64], int col0,
+                                          int row0, int lane)
+{
+#pragma unroll
+    for (int c = 0; c < 128 / CST_COLS; ++c) {
+        if (lane == 0)
+            bulk_wait_group_read0();   // the previous store has finished reading the buffer
+        __syncwarp();
+        const int w = c * (CST_COLS / 2);
+        st_shared_v4(buf + lane * 32, pk[w], pk[w + 1], pk[w + 2], pk[w + 3]);
+        st_shared_v4(buf + lane * 32 + 16, pk[w + 4], pk[w + 5], pk[w + 6], pk[w + 7]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, buf, col0 + c * CST_COLS, row0);
+            bulk_commit_group();
+        }
+    }
 }
 
 // Output tile t of the persistent schedule: groups of n_group N-tiles x all
@@ -163,9 +205,9 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
 
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const uint8_t *__restrict__ a_sf, const uint8_t *__restrict__ b_sf,
-                     const float *__restrict__ a_ts, const float *__restrict__ b_ts, uint16_t *__restrict__ C,
-                     int64_t ldc, int m, int n, int k, int m_tiles, int n_tiles, int n_group)
+                     const __grid_constant__ CUtensorMap tmC, const uint8_t *__restrict__ a_sf,
+                     const uint8_t *__restrict__ b_sf, const float *__restrict__ a_ts,
+                     const float *__restrict__ b_ts, int m, int n, int k, int m_tiles, int n_tiles, int n_group)
 {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -187,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
@@ -333,16 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&sm.acc_empty));   // accumulator free for the next tile
-
-            const int row = mt * BM + q * 32 + lane;
-            const int col0 = nt * BN + half * 128;
-            if (row < m && col0 < n) {
-                uint4 *dst = reinterpret_cast<uint4 *>(C + static_cast<int64_t>(row) * ldc + col0);
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
+            store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpiWarp]), pk, nt * BN + half * 128, mt * BM + q * 32,
+                       lane);
         }
+        if (lane == 0)
+            bulk_wait_group0();
     }
 
     tc_fence_before();
@@ -359,23 +397,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 // its own 128 rows (output columns) of B per K step, plus its 128 rows of A
 // scales and all 256 rows of B scales; the leader CTA (rank 0) issues the pair
 // MMA (M = 256) whose accumulator rows 0-127 land in the leader's TMEM and
-// rows 128-255 in the peer's.  Per SM and K step this moves 38 KB instead of
-// 54 KB for the same MMA work, so the ring holds 5 stages.
+// rows 128-255 in the peer's.  (Each CTA's rows read their A scales and all
+// 256 columns' B scales from that CTA's own TMEM, so both CTAs stage the full
+// B scales.)  Per SM and K step this moves 38 KB instead of 54 KB for the same
+// MMA work.  The 32 KB of A and B sit in a 6-stage ring; the 6 KB of scales
+// in a 4-slot shared-memory ring of their own and then in 5 TMEM slots.
 //   - Both CTAs' A and B loads complete on the leader's full barrier (the
 //     peer's through the cta_group::2 form of the tensor copy).  Each CTA's
-//     scale atoms complete on its own sf_full barrier; its scale warps stage
-//     them in its own TMEM and arrive on the leader's sf_ready barrier (8
-//     arrivals: 4 warps x 2 CTAs).  The MMA thread waits on full and sf_ready.
-//   - The leader's commits arrive on the barrier of both CTAs (multicast):
-//     a stage is free in both CTAs once the pair's MMAs have read it.
-//   - Each CTA's epilogue drains its own accumulator rows and arrives on the
-//     leader's accumulator-empty barrier (16 arrivals: 8 warps x 2 CTAs).
+//     scale atoms complete on its own sf_full barrier; its scale warps read
+//     them into registers (freeing the slot through sf_empty), wait until the
+//     MMAs that last used their TMEM slot completed (sf_free), stage them and
+//     arrive on the leader's sf_ready barrier (8 arrivals: 4 warps x 2 CTAs,
+//     relaxed: a cluster-scope release measured at 1,500 cycles per arrive).
+//     The MMA thread waits on full and sf_ready.
+//   - The leader's commits arrive on the barriers of both CTAs (multicast):
+//     an A/B stage and a TMEM scale slot are free in both CTAs once the pair's
+//     MMAs have read them.
+//   - Each CTA's epilogue drains its own accumulator rows, arrives on the
+//     leader's accumulator-empty barrier (16 arrivals: 8 warps x 2 CTAs) and
+//     writes its rows with tensor stores as in the single-CTA kernel.
 // ---------------------------------------------------------------------------
 namespace pair {
 
 constexpr int BM = 128;                    // rows per CTA; the pair covers 256
 constexpr int BN = 256;                    // output columns per pair tile
-constexpr int kStages = 5;
+constexpr int kStages = 6;                 // A/B ring
+constexpr int kSfSlots = 4;                // shared-memory scale ring
+constexpr int kTmemSlots = 5;              // TMEM scale slots (48 columns each, from column 256)
 constexpr uint32_t A_BYTES = BM * BKB;     // 16 KB
 constexpr uint32_t B_BYTES = 128 * BKB;    // 16 KB: this CTA's half of the B tile
 constexpr uint32_t SFA_BYTES = 4 * ATOM;   // this CTA's 128 rows x 16 scales
@@ -385,13 +433,16 @@ constexpr uint32_t SF_ROW = 256;           // row length of the scale tensor map
 struct __align__(1024) Smem {
     uint8_t a[kStages][A_BYTES];
     uint8_t b[kStages][B_BYTES];
-    uint8_t sfa[kStages][SFA_BYTES];
-    uint8_t sfb[kStages][SFB_BYTES];
-    uint64_t full[kStages];      // leader: both CTAs' A and B tiles landed
-    uint64_t sf_full[kStages];   // this CTA's scale atoms landed
-    uint64_t empty[kStages];     // both CTAs, arrived by the leader's commits
-    uint64_t sf_ready[kStages];  // leader: both CTAs' scales staged in TMEM
-    uint64_t acc_full;           // both CTAs
+    uint8_t sfa[kSfSlots][SFA_BYTES];
+    uint8_t sfb[kSfSlots][SFB_BYTES];
+    uint8_t cst[kEpiWarps][CST_BYTES];  // per epilogue warp: output staging for tensor stores
+    uint64_t full[kStages];          // leader: both CTAs' A and B tiles landed
+    uint64_t empty[kStages];         // both CTAs, arrived by the leader's commits
+    uint64_t sf_full[kSfSlots];      // this CTA's scale atoms landed
+    uint64_t sf_empty[kSfSlots];     // this CTA's scale warps have read a slot
+    uint64_t sf_ready[kTmemSlots];   // leader: both CTAs' scales staged in a TMEM slot
+    uint64_t sf_free[kTmemSlots];    // both CTAs: the MMAs reading a TMEM slot completed
+    uint64_t acc_full;               // both CTAs
     uint64_t acc_empty;          // used in the leader
     uint32_t tmem_base;
 };
@@ -400,9 +451,9 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                          const float *__restrict__ a_ts, const float *__restrict__ b_ts, uint16_t *__restrict__ C,
-                          int64_t ldc, int m, int n, int k, int m_tiles2, int n_tiles, int n_group, int sfa_rbs,
-                          int sfb_rbs)
+                          const __grid_constant__ CUtensorMap tmC, const float *__restrict__ a_ts,
+                          const float *__restrict__ b_ts, int m, int n, int k, int m_tiles2, int n_tiles, int n_group,
+                          int sfa_rbs, int sfb_rbs)
 {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -416,9 +467,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
-            mbar_init(smem_u32(&sm.sf_full[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), 1);
+        }
+        for (int s = 0; s < kSfSlots; ++s) {
+            mbar_init(smem_u32(&sm.sf_full[s]), 1);
+            mbar_init(smem_u32(&sm.sf_empty[s]), kScaleWarps);
+        }
+        for (int s = 0; s < kTmemSlots; ++s) {
             mbar_init(smem_u32(&sm.sf_ready[s]), 2 * kScaleWarps);
+            mbar_init(smem_u32(&sm.sf_free[s]), 1);
         }
         mbar_init(smem_u32(&sm.acc_full), 1);
         mbar_init(smem_u32(&sm.acc_empty), 2 * kEpiWarps);
@@ -427,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmSFA);
         prefetch_tmap(&tmSFB);
+        prefetch_tmap(&tmC);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(&sm.tmem_base), TMEM_COLS);
@@ -451,19 +509,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
-                    if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ph ^ 1u, kWaitLimitNs)) {
+                    const int f = it % kSfSlots;
+                    if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ph ^ 1u, kWaitLimitNs) ||
+                        !mbar_wait_bounded(smem_u32(&sm.sf_empty[f]), ((it / kSfSlots) & 1) ^ 1u, kWaitLimitNs)) {
                         record_error(ERR_WAIT_EMPTY);
                         ok = false;
                         break;
                     }
                     // scales first, on this CTA's own barrier (its scale warps stage them)
-                    const uint32_t sbar = smem_u32(&sm.sf_full[s]);
+                    const uint32_t sbar = smem_u32(&sm.sf_full[f]);
                     mbar_arrive_expect_tx(sbar, sf_tx);
                     if (has_sfa)
-                        tma_load_2d(smem_u32(sm.sfa[s]), &tmSFA, 0, (rb_a * chunks_per_rb + kt) * 8, sbar);
-                    tma_load_2d(smem_u32(sm.sfb[s]), &tmSFB, 0, (2 * nt * chunks_per_rb + kt) * 8, sbar);
+                        tma_load_2d(smem_u32(sm.sfa[f]), &tmSFA, 0, (rb_a * chunks_per_rb + kt) * 8, sbar);
+                    tma_load_2d(smem_u32(sm.sfb[f]), &tmSFB, 0, (2 * nt * chunks_per_rb + kt) * 8, sbar);
                     if (has_b1)
-                        tma_load_2d(smem_u32(sm.sfb[s]) + SFB_BYTES / 2, &tmSFB, 0,
+                        tma_load_2d(smem_u32(sm.sfb[f]) + SFB_BYTES / 2, &tmSFB, 0,
                                     ((2 * nt + 1) * chunks_per_rb + kt) * 8, sbar);
                     // A and B halves of both CTAs complete on the leader's full barrier
                     if (rank == 0)
@@ -488,15 +548,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
+                    const int ts = it % kTmemSlots;
                     // both CTAs' A and B landed and both CTAs' scales are in TMEM
                     if (!mbar_wait_bounded(smem_u32(&sm.full[s]), ph, kWaitLimitNs) ||
-                        !mbar_wait_bounded(smem_u32(&sm.sf_ready[s]), ph, kWaitLimitNs)) {
+                        !mbar_wait_bounded(smem_u32(&sm.sf_ready[ts]), (it / kTmemSlots) & 1, kWaitLimitNs)) {
                         record_error(ERR_WAIT_FULL);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem + SF_COL + s * SF_COLS_PER_STAGE;
+                    const uint32_t sfa_t = tmem + SF_COL + ts * SF_COLS_PER_STAGE;
                     const uint32_t sfb_t = sfa_t + 16;
                     const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, 1024, 2);
                     const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, 1024, 2);
@@ -505,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_nvf4_pair(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, idesc, sfa_t + 4 * j,
                                          sfb_t + 8 * j, (kt | j) != 0);
                     tc_commit_pair_mc(smem_u32(&sm.empty[s]), 0x3);
+                    tc_commit_pair_mc(smem_u32(&sm.sf_free[ts]), 0x3);
                 }
                 if (ok)
                     tc_commit_pair_mc(smem_u32(&sm.acc_full), 0x3);
@@ -512,27 +574,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kFirstScaleWarp) {
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t leader_sf_ready = mapa_shared(smem_u32(&sm.sf_ready[0]), 0);
         uint32_t it = 0;
-        for (int t = pair_id; t < total_tiles; t += num_pairs) {
-            bool ok = true;
+        bool ok = true;
+        for (int t = pair_id; t < total_tiles && ok; t += num_pairs) {
             for (int kt = 0; kt < kt_count; ++kt, ++it) {
-                const int s = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
-                if (!warp_wait(smem_u32(&sm.sf_full[s]), ph)) {
+                const int f = it % kSfSlots;
+                const int ts = it % kTmemSlots;
+                if (!warp_wait(smem_u32(&sm.sf_full[f]), (it / kSfSlots) & 1)) {
                     if (lane == 0)
                         record_error(ERR_WAIT_SCALES);
                     ok = false;
                     break;
                 }
-                stage_scales(tmem + lane_base, SF_COL + s * SF_COLS_PER_STAGE, SF_COL + s * SF_COLS_PER_STAGE + 16,
-                             sm.sfa[s], sm.sfb[s], lane);
-                tc_fence_before();
+                uint32_t a[16], b[32];
+                read_scales(sm.sfa[f], sm.sfb[f], lane, a, b);
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&sm.sf_ready[s]), 0));
+                    mbar_arrive(smem_u32(&sm.sf_empty[f]));   // the values are in registers
+                // the pair's MMAs that last read this TMEM slot have completed
+                if (!warp_wait(smem_u32(&sm.sf_free[ts]), ((it / kTmemSlots) & 1) ^ 1u)) {
+                    if (lane == 0)
+                        record_error(ERR_WAIT_SCALES);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st_32x32b_x16(tmem + lane_base + SF_COL + ts * SF_COLS_PER_STAGE, a);
+                tmem_st_32x32b_x32(tmem + lane_base + SF_COL + ts * SF_COLS_PER_STAGE + 16, b);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)   // relaxed: only tcgen05 stores are handed off, ordered by the fences
+                    mbar_arrive_cluster_relaxed(leader_sf_ready + ts * 8);
             }
-            if (!ok)
-                break;
         }
     } else {
         const int q = warp & 3;
@@ -575,16 +650,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)   // this CTA's rows are drained (relaxed: earlier tiles' stores need not land first)
                 mbar_arrive_cluster_relaxed(leader_acc_empty);
-
-            const int row = mt2 * 256 + static_cast<int>(rank) * BM + q * 32 + lane;
-            const int col0 = nt * BN + half * 128;
-            if (row < m && col0 < n) {
-                uint4 *dst = reinterpret_cast<uint4 *>(C + static_cast<int64_t>(row) * ldc + col0);
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
+            store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpiWarp]), pk, nt * BN + half * 128,
+                       mt2 * 256 + static_cast<int>(rank) * BM + q * 32, lane);
         }
+        if (lane == 0)
+            bulk_wait_group0();
     }
 
     tc_fence_before();
@@ -629,6 +699,23 @@ bool make_operand_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t k
     return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor map over the output C [m, n] with row stride ldc elements,
+// box 16 columns x 32 rows (one epilogue warp's store), no swizzle.
+bool make_output_map(CUtensorMap *tm, void *base, int64_t m, int64_t n, int64_t ldc)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc * 2)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(CST_COLS), 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 2-D uint8 tensor map viewing a scale buffer of `bytes` bytes as rows of 256
 // bytes, box 256 x 8 (one 2 KB chunk = 4 scale atoms), no swizzle.
 bool make_scale_map(CUtensorMap *tm, const void *base, int64_t bytes)
@@ -651,9 +738,10 @@ h3fp4_status launch_pair(const uint8_t *a_q, const uint8_t *a_sf, const float *a
                          int64_t n, int64_t k, int n_group_cfg, cudaStream_t st)
 {
     const int64_t sfa_rows = (m_pad + 127) / 128 * 128, sfb_rows = (n + 127) / 128 * 128;
-    CUtensorMap tmA, tmB, tmSFA, tmSFB;
+    CUtensorMap tmA, tmB, tmSFA, tmSFB, tmC;
     if (!make_operand_map(&tmA, a_q, m_pad, k / 2, pair::BM) || !make_operand_map(&tmB, b_q, n, k / 2, 128) ||
-        !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16)) || !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16)))
+        !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16)) || !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16)) ||
+        !make_output_map(&tmC, c, m, n, ldc))
         return H3FP4_ERR_CUDA;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -687,8 +775,8 @@ h3fp4_status launch_pair(const uint8_t *a_q, const uint8_t *a_sf, const float *a
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&lc, pair::nvf4_gemm_pair_kernel, tmA, tmB, tmSFA, tmSFB, a_ts, b_ts, c,
-                                             ldc, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k),
+    const cudaError_t e = cudaLaunchKernelEx(&lc, pair::nvf4_gemm_pair_kernel, tmA, tmB, tmSFA, tmSFB, tmC, a_ts, b_ts,
+                                             static_cast<int>(m), static_cast<int>(n), static_cast<int>(k),
                                              m_tiles2, n_tiles, n_group, static_cast<int>(sfa_rows / 128),
                                              static_cast<int>(sfb_rows / 128));
     return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
@@ -704,8 +792,9 @@ h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a
         return H3FP4_OK;
     if (cfg.cta_pair == 2)
         return launch_pair(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, st);
-    CUtensorMap tmA, tmB;
-    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, BM) || !make_operand_map(&tmB, b_q, n, k / 2, BN))
+    CUtensorMap tmA, tmB, tmC;
+    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, BM) || !make_operand_map(&tmB, b_q, n, k / 2, BN) ||
+        !make_output_map(&tmC, c, m, n, ldc))
         return H3FP4_ERR_CUDA;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -726,9 +815,9 @@ h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a
     if (n_group > n_tiles)
         n_group = n_tiles;
     const int grid = static_cast<int>(total < sm_count() ? total : sm_count());
-    nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, a_sf, b_sf, a_ts, b_ts, c, ldc,
-                                                        static_cast<int>(m), static_cast<int>(n),
-                                                        static_cast<int>(k), m_tiles, n_tiles, n_group);
+    nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, tmC, a_sf, b_sf, a_ts, b_ts, static_cast<int>(m),
+                                                        static_cast<int>(n), static_cast<int>(k), m_tiles, n_tiles,
+                                                        n_group);
     return cudaGetLastError() == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
 }
 
