@@ -147,7 +147,7 @@ h3fp4_status h3fp4_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_
     h3fp4_gemm_config c = {0, 0, 0, 0};
     if (cfg != nullptr) {
         c = *cfg;
-        if (c.n_group < 0 || c.stages != 0 || c.cta_pair < 0 || c.cta_pair > 2 || c.reserved != 0)
+        if (c.n_group < 0 || c.stages != 0 || c.cta_pair < 0 || c.cta_pair > 3 || c.reserved != 0)
             return H3FP4_ERR_UNSUPPORTED;
     }
     return h3fp4::launch_gemm(a_q, a_sf, a_tensor_scale, b_q, b_sf, b_tensor_scale,

@@ -93,6 +93,29 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Multicast forms: the data lands at this shared offset in every CTA of the
+// cluster named in `mask`, and each destination CTA's mbarrier at offset `bar`
+// receives the complete_tx of its copy.
+__device__ __forceinline__ void tma_load_2d_mcast(uint32_t dst, const void *tmap, int32_t x, int32_t y, uint32_t bar,
+                                                  uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_mcast(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                                uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "h"(mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -161,6 +184,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// As tc_commit, but the arrival goes to the mbarrier at this shared offset in
+// every CTA of the cluster named in `mask`.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
 }
 
 // 32 lanes x 32 columns of 32-bit TMEM words: thread t of the warp receives the

@@ -148,7 +148,10 @@ typedef struct h3fp4_gemm_config {
     int32_t stages;    /* reserved, must be 0 (the pipeline depth is fixed per kernel) */
     /* GEMM kernel: 0 = library default, 1 = one CTA per 128 x 256 output tile
      * (4-stage ring), 2 = CTA pairs on two SMs per 256 x 256 tile (tcgen05
-     * cta_group::2, each SM loads half of A and half of B; 5-stage ring). */
+     * cta_group::2, each SM loads half of A and half of B; 6-stage ring),
+     * 3 = clusters of two CTAs on the two 128 x 256 tiles of one 256 x 256
+     * block, each loading its own A and half of the shared B tile, multicast
+     * into both (4-stage ring). */
     int32_t cta_pair;
     int32_t reserved;  /* must be 0 */
 } h3fp4_gemm_config;

@@ -115,7 +115,7 @@ def test_gemm_validation(L):
     assert call(cfg=ctypes.byref(bad)) == UNSUP
     bad = pkg.GemmConfig(0, 3, 0, 0)
     assert call(cfg=ctypes.byref(bad)) == UNSUP
-    bad = pkg.GemmConfig(0, 0, 3, 0)
+    bad = pkg.GemmConfig(0, 0, 4, 0)       # kernels are 0 (default) .. 3
     assert call(cfg=ctypes.byref(bad)) == UNSUP
 
 

@@ -16,9 +16,10 @@ from dit_modulate_absmax_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 CANARY16 = 0x7E7E
 
-# Both GEMM kernels: one CTA per 128 x 256 tile (cta_pair=1) and CTA pairs on
-# 256 x 256 tiles (cta_pair=2).
-KERNELS = {"single": 1, "pair": 2}
+# Every GEMM kernel: one CTA per 128 x 256 tile (cta_pair=1), CTA pairs on
+# 256 x 256 tiles (cta_pair=2) and two-CTA clusters sharing B by multicast
+# (cta_pair=3).
+KERNELS = {"single": 1, "pair": 2, "mcast": 3}
 
 
 @pytest.fixture(params=sorted(KERNELS), ids=sorted(KERNELS))
