@@ -108,35 +108,35 @@ __device__ __forceinline__ float rcp_approx(float x)
     return y;
 }
 
-// Correctly rounded bf16 silu(g) = g / (1 + e^-g) for one bf16 pattern.
-//  - g >= 8: g itself.  g - silu(g) < g e^-g <= 8 e^-8 < 2^-6, which is below
-//    half the bf16 spacing just under g (g >= 8), and shrinks faster than
-//    the spacing grows, so the correctly rounded result is g.
-//  - -16 <= g < 8: FP32 evaluation s = g * rcp(1 + 2^(g * -log2 e)).  The
-//    rounded exponent argument (|argument| <= 23.1) costs at most
-//    0.7 * 23.1 * 2^-23 < 2^-19 relative, the hardware exp2 and reciprocal
-//    approximations about 2^-22 each, the add and multiply 2^-24 each: less
-//    than 2^-18.6 in all.  So the exact silu lies between s (1 - 2^-17) and
-//    s (1 + 2^-17); bf16 rounding is monotone, so when both round to the same
-//    bf16 value that value is the correctly rounded silu.  Otherwise (a bf16
-//    rounding boundary within 2^-17 of s) the build-time table decides.
-//  - g < -16, |g| < 2^-100 (where s (1 +- 2^-17) can underflow to the same
-//    subnormal and the sandwich collapses) and NaN: the table.
-// Returns the FP32-path result; `unsure` is set when the table must decide.
-__device__ __forceinline__ uint32_t silu_bf16_fast(uint32_t gbits, bool &unsure)
+// Correctly rounded bf16 silu(g) = g / (1 + e^-g) for the two bf16 halves of
+// a word, in FP32 with packed two-lane arithmetic: s = g * rcp(1 + 2^(g *
+// -log2 e)).
+//  - g >= -16: the rounded exponent argument costs at most 0.7 * 23.1 *
+//    2^-23 < 2^-19 relative while e^-g is not negligible (|argument| <= 23.1
+//    for g in [-16, 16]; beyond, e^-g shrinks faster than the argument grows),
+//    the hardware exp2 and reciprocal approximations about 2^-22 each, the add
+//    and multiply 2^-24 each: |s - silu(g)| < 2^-18.5 |s| in all (for large g
+//    the exponent underflows to 0 and s = g exactly).  In ulps of s that is
+//    below 2^5.5, so RN_bf16(s) is the correctly rounded silu unless s lies
+//    within 128 ulps of a bf16 rounding midpoint (the low 16 bits of s within
+//    0x7F80 .. 0x807F); those values go to the table.
+//  - g < -16, |g| < 2^-100 (where s can leave the normal range) and NaN: the
+//    build-time table of correctly rounded values decides.
+// Returns both FP32-path results; bit 0 / bit 1 of `bad` flags the low / high
+// half for the table.
+__device__ __forceinline__ bool silu_needs_table(float g, float s)
 {
-    const float g = __uint_as_float(gbits << 16);
-    if (g >= 8.0f) {
-        unsure = false;
-        return gbits;
-    }
-    const float e = ex2_approx(__fmul_rn(g, -0x1.715476p+0f));
-    const float s = __fmul_rn(g, rcp_approx(__fadd_rn(1.0f, e)));
-    const __nv_bfloat162 both = __floats2bfloat162_rn(__fmul_rn(s, 1.0f - 0x1p-17f), __fmul_rn(s, 1.0f + 0x1p-17f));
-    uint32_t u;
-    memcpy(&u, &both, 4);
-    unsure = !(g >= -16.0f) || !(fabsf(g) >= 0x1p-100f) || ((u ^ (u >> 16)) & 0xFFFFu) != 0u;
-    return u & 0xFFFFu;
+    return (((__float_as_uint(s) - 0x7F80u) & 0xFFFFu) < 0x100u) || !(g >= -16.0f) || !(fabsf(g) >= 0x1p-100f);
+}
+
+__device__ __forceinline__ uint32_t silu2_fast(uint32_t gw, uint32_t &bad)
+{
+    const float2 g = make_float2(__uint_as_float(gw << 16), __uint_as_float(gw & 0xFFFF0000u));
+    const float2 a = __fmul2_rn(g, make_float2(-0x1.715476p+0f, -0x1.715476p+0f));
+    const float2 d = __fadd2_rn(make_float2(ex2_approx(a.x), ex2_approx(a.y)), make_float2(1.0f, 1.0f));
+    const float2 sv = __fmul2_rn(g, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+    bad = (silu_needs_table(g.x, sv.x) ? 1u : 0u) | (silu_needs_table(g.y, sv.y) ? 2u : 0u);
+    return as_u32(__floats2bfloat162_rn(sv.x, sv.y));
 }
 
 // ---------------------------------------------------------------------------
@@ -228,9 +228,9 @@ struct SwigluSrc {
         uint32_t unsure = 0;  // bit 2i / 2i+1: value needs the table
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            bool ulo, uhi;
-            sv[i] = silu_bf16_fast(gw[i] & 0xFFFFu, ulo) | (silu_bf16_fast(gw[i] >> 16, uhi) << 16);
-            unsure |= (ulo ? 1u : 0u) << (2 * i) | (uhi ? 1u : 0u) << (2 * i + 1);
+            uint32_t bad;
+            sv[i] = silu2_fast(gw[i], bad);
+            unsure |= bad << (2 * i);
         }
         while (unsure) {  // rare: each flagged value is looked up once
             const int e = __ffs(unsure) - 1;
@@ -375,18 +375,20 @@ __device__ __forceinline__ uint32_t block_scale(uint32_t bmax_bits, float den, f
 // signed zeros.
 //
 // The code of y is E2M1_RNE_sat(RN_f32(y / sc)).  Instead of one IEEE division
-// per value the block computes r = RN(1/sc) and two nudged reciprocals
-// r_lo = RN(r (1 - 2^-20)), r_hi = RN(r (1 + 2^-20)), and each value is
-// converted twice, from q_lo = RN(y r_lo) and q_hi = RN(y r_hi).  With
-// v = y/sc exact and sc, 1/sc normal, |y r - v| <= 2^-23 |v| up to rounding,
-// so |q_lo| < |v| (1 - 2^-21) < |RN_f32(v)| and |q_hi| > |RN_f32(v)|: the
-// correctly rounded quotient lies between q_lo and q_hi.  Rounding to E2M1 is
-// monotone, so where both conversions agree they give the code of
-// RN_f32(v) (quotients below the normal range round to a signed zero either
-// way).  Where they differ -- some rounding boundary lies within 2^-20 of the
-// quotient, a rare case -- those 8 values are redone with the IEEE division;
-// so are whole blocks whose sc lies outside [2^-125, 2^125].  The sign of y
-// (also of y = -0) carries through the products into the code.
+// per value the block computes r = rcp.approx(sc) (relative error at most
+// 2^-23; the argument below allows 2^-21) and two nudged reciprocals
+// r_lo = RN(r (1 - 2^-19)), r_hi = RN(r (1 + 2^-19)), and each value is
+// converted twice, from q_lo = RN(y r_lo) and q_hi = RN(y r_hi) (packed
+// two-lane products).  With v = y/sc exact and sc, 1/sc normal,
+// r_lo <= (1/sc)(1 + 2^-21 - 2^-19 + 2^-24) < (1/sc)(1 - 2^-20), so
+// |q_lo| < |v| (1 - 2^-21) < |RN_f32(v)|, and symmetrically |q_hi| >
+// |RN_f32(v)|: the correctly rounded quotient lies between q_lo and q_hi.
+// Rounding to E2M1 is monotone, so where both conversions agree they give the
+// code of RN_f32(v) (quotients below the normal range round to a signed zero
+// either way).  Where they differ -- some rounding boundary lies within 2^-19
+// of the quotient, a rare case -- those 8 values are redone with the IEEE
+// division; so are whole blocks whose sc lies outside [2^-125, 2^125].  The
+// sign of y (also of y = -0) carries through the products into the code.
 __device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
 {
     if (sc == 0.0f) {
@@ -397,9 +399,10 @@ __device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
         return make_uint2(signs[0], signs[1]);
     }
     const bool normal_range = sc >= 0x1p-125f && sc <= 0x1p125f;
-    const float r = normal_range ? __frcp_rn(sc) : 0.0f;
-    const float r_lo = __fmul_rn(r, 1.0f - 0x1p-20f);
-    const float r_hi = __fmul_rn(r, 1.0f + 0x1p-20f);
+    const float r = normal_range ? rcp_approx(sc) : 0.0f;
+    const float r_lo = __fmul_rn(r, 1.0f - 0x1p-19f);
+    const float r_hi = __fmul_rn(r, 1.0f + 0x1p-19f);
+    const float2 rl2 = make_float2(r_lo, r_lo), rh2 = make_float2(r_hi, r_hi);
     uint32_t out[2];
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {   // 8 values (4 words) at a time
@@ -407,9 +410,10 @@ __device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t w = y[4 * hlf + i];
-            const float a0 = __uint_as_float(w << 16), a1 = __uint_as_float(w & 0xFFFF0000u);
-            const uint32_t b_lo = cvt_e2m1x2(__fmul_rn(a1, r_lo), __fmul_rn(a0, r_lo));
-            const uint32_t b_hi = cvt_e2m1x2(__fmul_rn(a1, r_hi), __fmul_rn(a0, r_hi));
+            const float2 a = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+            const float2 ql = __fmul2_rn(a, rl2), qh = __fmul2_rn(a, rh2);
+            const uint32_t b_lo = cvt_e2m1x2(ql.y, ql.x);
+            const uint32_t b_hi = cvt_e2m1x2(qh.y, qh.x);
             diff |= b_lo ^ b_hi;
             lo |= b_lo << (8 * i);
         }
