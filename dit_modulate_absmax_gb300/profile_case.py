@@ -1,9 +1,11 @@
 """Runs one hot-path call on synthetic inputs, for profilers.
 
   python -m dit_modulate_absmax_gb300.profile_case {modulate,swiglu,gemm} [--m M] [--n N] [--k K] [--reps R]
+      [--workspace] [--cta-pair P] [--n-group G]
 
 `modulate` runs both passes of the modulation producer on an [M, K]
-activation, `swiglu` the SwiGLU producer on [M, K] gate/up, `gemm` the
+activation, `swiglu` the SwiGLU producer on [M, K] gate/up (with
+`--workspace`, the form the benchmark times: pass 1 keeps h), `gemm` the
 block-scaled GEMM of a packed [M, K] activation with a packed [N, K] weight.
 The R timed repetitions run between cudaProfilerStart and cudaProfilerStop
 (so `ncu --profile-from-start off` sees only them) after two warm-up calls,
@@ -30,6 +32,8 @@ def main():
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--cta-pair", type=int, default=0, help="GEMM kernel: 0 default, 1 single CTA, 2 CTA pairs")
     ap.add_argument("--n-group", type=int, default=0, help="GEMM N-group (0 = default)")
+    ap.add_argument("--workspace", action="store_true",
+                    help="swiglu: keep h in a workspace (pass 1 writes it, pass 2 packs from it)")
     a = ap.parse_args()
     B.build()
     dev = torch.device("cuda")
@@ -44,8 +48,11 @@ def main():
     q = torch.empty(m_pad, a.k // 2, dtype=torch.uint8, device=dev)
     sfa = torch.empty(h3.sf_bytes(m_pad, a.k), dtype=torch.uint8, device=dev)
     if a.op == "swiglu":
+        hw = torch.empty(a.m, a.k, dtype=torch.int16, device=dev) if a.workspace else None
+
         def call():
-            h3.swiglu_pack(act["gate"], act["up"], m_pad, tensor_scale=ts, scratch=scratch, qdata=q, sfa=sfa)
+            h3.swiglu_pack(act["gate"], act["up"], m_pad, h_workspace=hw, tensor_scale=ts, scratch=scratch, qdata=q,
+                           sfa=sfa)
     else:
         def produce():
             h3.modulate_absmax(act["x"], act["shift"], act["scale"], off, tensor_scale=ts, scratch=scratch)
