@@ -173,7 +173,7 @@ def _bytes_per_element(kind):
 
 
 class Linear:
-    def __init__(self, h3, W, name, dev):
+    def __init__(self, h3, W, name, dev, gemm_kernel=0):
         import torch
         self.h3, self.name = h3, name
         self.w = w = W.WORKLOADS[name]
@@ -194,6 +194,7 @@ class Linear:
         self.flops = 2.0 * w.m * w.n * w.k
         self.prod_bytes = _bytes_per_element(w.kind) * w.m * w.k
         self.launches = 3          # absmax kernel, pack kernel, GEMM kernel
+        self.cfg = h3.GemmConfig(0, 0, gemm_kernel, 0) if gemm_kernel else None
         self.ev = None
 
     def inputs(self):
@@ -211,7 +212,7 @@ class Linear:
                            scratch=self.scratch, qdata=self.q, sfa=self.sfa)
         if events is not None:
             events[1].record()
-        h3.gemm(self.q, self.sfa, self.ts, self.bq, self.bsf, self.bts, w.m, out=self.c)
+        h3.gemm(self.q, self.sfa, self.ts, self.bq, self.bsf, self.bts, w.m, out=self.c, cfg=self.cfg)
         if events is not None:
             events[2].record()
 
@@ -231,7 +232,7 @@ def run_ours(args, rank, world, local_rank):
     h3.lib()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    lins = [Linear(h3, W, n, dev) for n in LINEARS]
+    lins = [Linear(h3, W, n, dev, args.gemm_kernel) for n in LINEARS]
     torch.cuda.synchronize()
 
     def step(ev=None):
@@ -411,6 +412,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=128)
     ap.add_argument("--cpu-cols", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-kernel", type=int, default=0, choices=(0, 1, 2, 3),
+                    help="GEMM kernel (h3fp4_gemm_config.cta_pair): 0 library default, 1 single CTA, "
+                         "2 CTA pair, 3 two-CTA cluster with B multicast")
     ap.add_argument("--profile-range", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()

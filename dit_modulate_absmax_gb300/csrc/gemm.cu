@@ -840,7 +840,7 @@ h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a
         return H3FP4_OK;
     if (cfg.cta_pair == 2)
         return launch_pair(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, st);
-    const bool mcast = cfg.cta_pair == 3;
+    const bool mcast = cfg.cta_pair == 3 || cfg.cta_pair == 0;   // the default: measured fastest in the DiT step
     CUtensorMap tmA, tmB, tmC;
     if (!make_operand_map(&tmA, a_q, m_pad, k / 2, BM) ||
         !make_operand_map(&tmB, b_q, n, k / 2, mcast ? BN / 2 : BN) || !make_output_map(&tmC, c, m, n, ldc))

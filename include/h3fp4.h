@@ -146,7 +146,7 @@ typedef struct h3fp4_gemm_config {
      * clamped). */
     int32_t n_group;
     int32_t stages;    /* reserved, must be 0 (the pipeline depth is fixed per kernel) */
-    /* GEMM kernel: 0 = library default, 1 = one CTA per 128 x 256 output tile
+    /* GEMM kernel: 0 = library default (currently 3), 1 = one CTA per 128 x 256 output tile
      * (4-stage ring), 2 = CTA pairs on two SMs per 256 x 256 tile (tcgen05
      * cta_group::2, each SM loads half of A and half of B; 6-stage ring),
      * 3 = clusters of two CTAs on the two 128 x 256 tiles of one 256 x 256
