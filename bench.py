@@ -35,9 +35,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "producer GB/s & NVFP4 GEMM TFLOP/s vs roofline at M=37,810 rows (ms/linear)"
 UNIT = "ms/linear"
-LINEARS = ("qkv", "fc1", "fc2")
-WORKLOAD = ("DiT block NVFP4 linears at M=37,810 (padded 37,824): qkv K=7168 N=21504, "
-            "fc1 K=7168 N=14336 (fused modulate producer), fc2 K=14336 N=7168 (SwiGLU producer)")
+# Linear sets: the default (the benchmark's configs) and the model's own projection widths.
+WIDTHS = {
+    "baseline": (("qkv", "fc1", "fc2"),
+                 "DiT block NVFP4 linears at M=37,810 (padded 37,824): qkv K=7168 N=21504, "
+                 "fc1 K=7168 N=14336 (fused modulate producer), fc2 K=14336 N=7168 (SwiGLU producer)"),
+    "h3": (("h3_qkv", "h3_attn", "h3_fc1", "h3_fc2"),
+           "DiT block NVFP4 linears at the model's own widths, M=37,810 (padded 37,824): qkv K=5376 N=21504, "
+           "attention output K=7168 N=5376 (plain producer), fc1 K=5376 N=14336 (fused modulate producer), "
+           "fc2 K=14336 N=5376 (SwiGLU producer)"),
+}
+LINEARS, WORKLOAD = WIDTHS["baseline"]
 FP4_PER_BF16 = 13.5 / 2.25   # nominal dense NVFP4 / BF16 tensor rate
 
 
@@ -169,7 +177,7 @@ def _bytes_per_element(kind):
     # producer algorithmic bytes per activation element: both passes read the bf16
     # input (SwiGLU: pass 1 reads gate and up and writes h, pass 2 reads h), pass 2
     # writes 0.5 B of QDATA and 1/16 B of scale
-    return (2 + 2 + 0.5 + 1 / 16) if kind == "modulate" else (4 + 2 + 2 + 0.5 + 1 / 16)
+    return (4 + 2 + 2 + 0.5 + 1 / 16) if kind == "swiglu" else (2 + 2 + 0.5 + 1 / 16)
 
 
 class Linear:
@@ -198,7 +206,7 @@ class Linear:
         self.ev = None
 
     def inputs(self):
-        return [self.act[k] for k in (("x",) if self.w.kind == "modulate" else ("gate", "up"))]
+        return [self.act[k] for k in (("gate", "up") if self.w.kind == "swiglu" else ("x",))]
 
     def run(self, events=None):
         h3, w, a = self.h3, self.w, self.act
@@ -207,6 +215,8 @@ class Linear:
         if w.kind == "modulate":
             h3.modulate_absmax(a["x"], a["shift"], a["scale"], self.off, tensor_scale=self.ts, scratch=self.scratch)
             h3.modulate_pack(a["x"], a["shift"], a["scale"], self.off, self.ts, w.m_pad, qdata=self.q, sfa=self.sfa)
+        elif w.kind == "plain":
+            h3.quantize_pack(a["x"], w.m_pad, tensor_scale=self.ts, scratch=self.scratch, qdata=self.q, sfa=self.sfa)
         else:
             h3.swiglu_pack(a["gate"], a["up"], w.m_pad, h_workspace=self.h, tensor_scale=self.ts,
                            scratch=self.scratch, qdata=self.q, sfa=self.sfa)
@@ -367,6 +377,8 @@ def cpu_baseline(rows=64, cols=2048, seed_device="cpu"):
         if w.kind == "modulate":
             ts, q, sf, _, _ = oracle.modulate_producer(act["x"].numpy(), act["shift"].numpy(),
                                                        act["scale"].numpy(), W.seg_offsets(w, rows), rows)
+        elif w.kind == "plain":
+            ts, q, sf, _ = oracle.plain_producer(act["x"].numpy(), rows)
         else:
             ts, q, sf, _, _ = oracle.swiglu_producer(act["gate"].numpy(), act["up"].numpy(), rows)
         t1 = time.perf_counter()
@@ -379,7 +391,7 @@ def cpu_baseline(rows=64, cols=2048, seed_device="cpu"):
         total_ms += ((t1 - t0) * w.m / rows + fixed * w.n / c + mm * (w.m / rows) * (w.n / c)) * 1e3
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": round(total_ms / len(LINEARS), 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{rows} activation rows x {cols} weight rows of each of qkv/fc1/fc2; producer time "
+            "sample": f"{rows} activation rows x {cols} weight rows of each of {'/'.join(LINEARS)}; producer time "
                       f"scaled by M/rows, per-column GEMM work by N/cols, FP64 products by both; C loops on "
                       f"one core, FP64 matmul through numpy BLAS threads"}
 
@@ -412,12 +424,16 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=128)
     ap.add_argument("--cpu-cols", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--widths", choices=sorted(WIDTHS), default="baseline",
+                    help="linear set: the benchmark's configs (default) or the model's own projection widths")
     ap.add_argument("--gemm-kernel", type=int, default=0, choices=(0, 1, 2, 3),
                     help="GEMM kernel (h3fp4_gemm_config.cta_pair): 0 library default, 1 single CTA, "
                          "2 CTA pair, 3 two-CTA cluster with B multicast")
     ap.add_argument("--profile-range", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()
+    global LINEARS, WORKLOAD
+    LINEARS, WORKLOAD = WIDTHS[args.widths]
     args.warmup = max(args.warmup, 3)
     rank = _env_int("RANK", 0)
     world = _env_int("WORLD_SIZE", 1)

@@ -27,6 +27,7 @@ _SIGNATURES = {
     "h3fp4_modulate_absmax": ([_P, _I64, _I64, _I64, _P, _P, _I64, _P, _I32, _P, _P, _P], _STATUS),
     "h3fp4_modulate_pack": ([_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _I32, _P, _P, _P, _P], _STATUS),
     "h3fp4_swiglu_pack": ([_P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P], _STATUS),
+    "h3fp4_quantize_pack": ([_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P], _STATUS),
     "h3fp4_gemm": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P], _STATUS),
     "h3fp4_swizzle_scales": ([_P, _I64, _I64, _I64, _P, _P], _STATUS),
     "h3fp4_swiglu_pack_noalloc": ([_P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P], _STATUS),
@@ -104,6 +105,10 @@ def h3fp4_swiglu_pack(gate, ldg, up, ldu, m, m_pad, f, tensor_scale, scratch, qd
                       stream=0):
     _call("h3fp4_swiglu_pack", gate, ldg, up, ldu, m, m_pad, f, tensor_scale, scratch, qdata, sfa, h_workspace,
           stream)
+
+
+def h3fp4_quantize_pack(x, ldx, m, m_pad, d, tensor_scale, scratch, qdata, sfa, stream=0):
+    _call("h3fp4_quantize_pack", x, ldx, m, m_pad, d, tensor_scale, scratch, qdata, sfa, stream)
 
 
 def h3fp4_gemm(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg: GemmConfig | None = None, stream=0):
@@ -202,6 +207,25 @@ def swiglu_pack(gate, up, m_pad, *, h_workspace=None, tensor_scale=None, scratch
     h3fp4_swiglu_pack(gate.data_ptr(), gate.stride(0), up.data_ptr(), up.stride(0), m, m_pad, f,
                       tensor_scale.data_ptr(), scratch.data_ptr(), qdata.data_ptr(), sfa.data_ptr(),
                       h_workspace.data_ptr() if h_workspace is not None else None, _stream(stream))
+    return tensor_scale, qdata, sfa
+
+
+def quantize_pack(x, m_pad, *, tensor_scale=None, scratch=None, qdata=None, sfa=None, stream=None):
+    """NVFP4 producer of a plain bf16 activation (both passes): returns (tensor_scale, qdata, sfa)."""
+    import torch
+    _need_cuda(x)
+    m, d = x.shape
+    dev = x.device
+    if tensor_scale is None:
+        tensor_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    if scratch is None:
+        scratch = torch.empty(2, dtype=torch.int32, device=dev)
+    if qdata is None:
+        qdata = torch.empty(m_pad, d // 2, dtype=torch.uint8, device=dev)
+    if sfa is None:
+        sfa = torch.empty(sf_bytes(m_pad, d), dtype=torch.uint8, device=dev)
+    h3fp4_quantize_pack(x.data_ptr(), x.stride(0), m, m_pad, d, tensor_scale.data_ptr(), scratch.data_ptr(),
+                        qdata.data_ptr(), sfa.data_ptr(), _stream(stream))
     return tensor_scale, qdata, sfa
 
 

@@ -131,6 +131,22 @@ h3fp4_status h3fp4_swiglu_pack(const void *gate_bf16, int64_t ldg, const void *u
         tensor_scale, scratch, qdata, sfa, static_cast<uint16_t *>(h_workspace), as_stream(stream)));
 }
 
+h3fp4_status h3fp4_quantize_pack(const void *x_bf16, int64_t ldx, int64_t m, int64_t m_pad, int64_t d,
+                                 float *tensor_scale, uint32_t *scratch, uint8_t *qdata, uint8_t *sfa, void *stream)
+{
+    if ((x_bf16 == nullptr && m != 0) || tensor_scale == nullptr || scratch == nullptr)
+        return H3FP4_ERR_NULL;
+    if (m < 0 || m > INT32_MAX || d <= 0 || d % 256 != 0 || d > (int64_t(1) << 24) || ldx < d)
+        return H3FP4_ERR_SHAPE;
+    if (!aligned16(x_bf16) || ldx % 8 != 0)
+        return H3FP4_ERR_ALIGN;
+    h3fp4_status s = check_pack_outputs(m, m_pad, qdata, sfa);
+    if (s != H3FP4_OK)
+        return s;
+    return from_cuda(h3fp4::launch_quantize_pack(static_cast<const uint16_t *>(x_bf16), ldx, m, m_pad, d,
+                                                 tensor_scale, scratch, qdata, sfa, as_stream(stream)));
+}
+
 h3fp4_status h3fp4_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_tensor_scale, const uint8_t *b_q,
                         const uint8_t *b_sf, const float *b_tensor_scale, void *c_bf16, int64_t ldc, int64_t m,
                         int64_t m_pad, int64_t n, int64_t k, const h3fp4_gemm_config *cfg, void *stream)

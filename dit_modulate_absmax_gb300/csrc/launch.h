@@ -30,6 +30,9 @@ cudaError_t launch_swiglu_pack(const uint16_t *gate, int64_t ldg, const uint16_t
                                int64_t m, int64_t m_pad, int64_t f, float *ts, uint32_t *scratch,
                                uint8_t *qdata, uint8_t *sf, uint16_t *h, cudaStream_t st);
 
+cudaError_t launch_quantize_pack(const uint16_t *x, int64_t ldx, int64_t m, int64_t m_pad, int64_t d,
+                                 float *ts, uint32_t *scratch, uint8_t *qdata, uint8_t *sf, cudaStream_t st);
+
 cudaError_t launch_swizzle_scales(const uint8_t *src, int64_t rows, int64_t cols, int64_t ld,
                                   uint8_t *dst, cudaStream_t st);
 

@@ -581,6 +581,16 @@ cudaError_t launch_modulate_pack(const uint16_t *x, int64_t ldx, int64_t m, int6
     return run_pack(src, m, m_pad, d, ts, qdata, sf, st);
 }
 
+cudaError_t launch_quantize_pack(const uint16_t *x, int64_t ldx, int64_t m, int64_t m_pad, int64_t d, float *ts,
+                                 uint32_t *scratch, uint8_t *qdata, uint8_t *sf, cudaStream_t st)
+{
+    PlainSrc src{x, ldx};
+    cudaError_t e = run_absmax(src, m, d, ts, scratch, st);
+    if (e != cudaSuccess)
+        return e;
+    return run_pack(src, m, m_pad, d, ts, qdata, sf, st);
+}
+
 cudaError_t launch_swiglu_pack(const uint16_t *gate, int64_t ldg, const uint16_t *up, int64_t ldu, int64_t m,
                                int64_t m_pad, int64_t f, float *ts, uint32_t *scratch, uint8_t *qdata, uint8_t *sf,
                                uint16_t *h, cudaStream_t st)

@@ -18,6 +18,15 @@ Workloads (one DiT block at the 37,810-token shape):
   MLP shift/scale, weights [14,336, 7,168].
 * ``fc2``      -- gate, up N(0,1) [37,810, 14,336], weights [7,168, 14,336].
 
+The model's own projection widths (hidden width 5,376, attention width 7,168,
+MLP width 14,336; QKV output 21,504) at the same 37,810 tokens:
+
+* ``h3_qkv``   -- as ``qkv`` with K=5,376.
+* ``h3_attn``  -- attention output: plain N(0,1) activations [37,810, 7,168]
+  (quantized without a fused transform), weights [5,376, 7,168].
+* ``h3_fc1``   -- as ``fc1`` with K=5,376.
+* ``h3_fc2``   -- as ``fc2`` with N=5,376.
+
 Weights (all but ``tiny``) use E4M3 codes for values 0.25 ... 8 and a weight
 tensor scale of 2^-10.
 """
@@ -34,7 +43,7 @@ M_PAD = 37_824
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "modulate" or "swiglu"
+    kind: str                 # "modulate", "swiglu" or "plain"
     m: int                    # logical rows
     m_pad: int                # descriptor rows (zero padded)
     k: int                    # producer width D (= GEMM K)
@@ -61,6 +70,12 @@ WORKLOADS = {
     "fc1": Workload("fc1", "modulate", M_TOKENS, M_PAD, 7168, 14_336,
                     (0, 32_768, M_TOKENS), seed=3, outlier_frac=0.001, outlier_std=30.0),
     "fc2": Workload("fc2", "swiglu", M_TOKENS, M_PAD, 14_336, 7_168, (), seed=4),
+    "h3_qkv": Workload("h3_qkv", "modulate", M_TOKENS, M_PAD, 5376, 21_504,
+                       (0, 32_768, M_TOKENS), seed=5, rms_rows=True),
+    "h3_attn": Workload("h3_attn", "plain", M_TOKENS, M_PAD, 7168, 5376, (), seed=6),
+    "h3_fc1": Workload("h3_fc1", "modulate", M_TOKENS, M_PAD, 5376, 14_336,
+                       (0, 32_768, M_TOKENS), seed=7, outlier_frac=0.001, outlier_std=30.0),
+    "h3_fc2": Workload("h3_fc2", "swiglu", M_TOKENS, M_PAD, 14_336, 5376, (), seed=8),
 }
 
 
@@ -77,9 +92,12 @@ def _bf16(t: torch.Tensor) -> torch.Tensor:
 
 def activations(w: Workload, device="cpu", m: int | None = None) -> dict:
     """Producer inputs as int16 bf16 patterns: x [m, k], shift/scale [nseg, k]
-    for modulate workloads; gate/up [m, k] for swiglu workloads."""
+    for modulate workloads; gate/up [m, k] for swiglu workloads; x [m, k] for
+    plain workloads."""
     m = w.m if m is None else m
     g = _gen(w.seed, device)
+    if w.kind == "plain":
+        return {"x": _bf16(torch.randn(m, w.k, generator=g, device=device, dtype=torch.float32))}
     if w.kind == "swiglu":
         gate = torch.randn(m, w.k, generator=g, device=device, dtype=torch.float32)
         up = torch.randn(m, w.k, generator=g, device=device, dtype=torch.float32)

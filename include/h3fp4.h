@@ -137,6 +137,28 @@ H3FP4_API h3fp4_status h3fp4_swiglu_pack(const void *gate_bf16, int64_t ldg, con
                                float *tensor_scale, uint32_t *scratch, uint8_t *qdata,
                                uint8_t *sfa, void *h_workspace, void *stream);
 
+/*
+ * h3fp4_quantize_pack -- NVFP4 producer of an activation that needs no fused
+ * transform (both passes).
+ * Source: "NVFP4 Modulation Producer Fusion", Change Summary (the same two-pass
+ * producer: global absmax -> FP32 tensor scale, then E4M3 block scales and
+ * E2M1 codes); "NVFP4 Streaming Design", P0 and P2 (the attention-output
+ * projection is one of the four H3 projections, its input quantized by the
+ * same rules without the modulation).
+ *
+ * amax = max |x| over the m logical rows, ts = RN_f32(amax / 2688), then the
+ * pack of x exactly as h3fp4_modulate_pack packs y.
+ *
+ *   x_bf16        [m, d] bf16, leading dimension ldx (multiple of 8), 16-byte aligned
+ *   d             multiple of 256
+ *   tensor_scale  1 float (output)
+ *   scratch       2 uint32 words (as for h3fp4_modulate_absmax)
+ *   qdata, sfa    as for h3fp4_modulate_pack
+ */
+H3FP4_API h3fp4_status h3fp4_quantize_pack(const void *x_bf16, int64_t ldx, int64_t m, int64_t m_pad,
+                                 int64_t d, float *tensor_scale, uint32_t *scratch, uint8_t *qdata,
+                                 uint8_t *sfa, void *stream);
+
 /* Tuning knobs of the GEMM; pass NULL for the defaults. */
 typedef struct h3fp4_gemm_config {
     /* N-group A-tile reuse factor: the persistent schedule walks the 128 x 256

@@ -254,6 +254,16 @@ def modulate_producer(x, shift, scale, seg_off, m_pad: int):
     return ts, q, sf, y, amax
 
 
+def plain_producer(x, m_pad: int):
+    """Both producer passes on an activation taken as it is (no fused transform):
+    returns (ts, qdata, sf_logical, amax_bits)."""
+    xs = _u16(x)
+    amax = absmax(xs)
+    ts = tensor_scale(amax)
+    q, sf = pack(xs, m_pad, ts)
+    return ts, q, sf, amax
+
+
 # ----------------------------------------------------------------------------
 # SwiGLU
 # ----------------------------------------------------------------------------

@@ -97,6 +97,15 @@ def test_swiglu_pack_validation(L):
     assert f(F, 256, F, 256, 10, 4, 256, F, F, F, F, None, None) == SHAPE
 
 
+def test_quantize_pack_validation(L):
+    f = L.h3fp4_quantize_pack
+    assert f(None, 256, 10, 16, 256, F, F, F, F, None) == NULL
+    assert f(F, 256, 10, 16, 300, F, F, F, F, None) == SHAPE       # d not a multiple of 256
+    assert f(F, 200, 10, 16, 256, F, F, F, F, None) == SHAPE       # ldx < d
+    assert f(F + 2, 256, 10, 16, 256, F, F, F, F, None) == ALIGN
+    assert f(F, 256, 10, 4, 256, F, F, F, F, None) == SHAPE         # m_pad < m
+
+
 def test_gemm_validation(L):
     f = L.h3fp4_gemm
 

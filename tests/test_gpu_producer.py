@@ -233,6 +233,55 @@ def test_swiglu_bit_exact(h3, m, m_pad, f, scale, workspace):
         assert np.array_equal(h, h_o)
 
 
+def run_plain(h3, x, m_pad, ldx=None):
+    m, d = x.shape
+    ld = d if ldx is None else ldx
+    buf = np.zeros((m, ld), dtype=np.uint16)
+    buf[:, :d] = x
+    xd = _to_dev(buf)[:, :d] if m else torch.empty(0, d, dtype=torch.int16, device="cuda")
+    q = torch.full((m_pad, d // 2), CANARY, dtype=torch.uint8, device="cuda")
+    sfa = torch.full((h3.sf_bytes(m_pad, d),), CANARY, dtype=torch.uint8, device="cuda")
+    ts = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    h3.quantize_pack(xd, m_pad, tensor_scale=ts, qdata=q, sfa=sfa)
+    torch.cuda.synchronize()
+    assert h3.h3fp4_device_error() == 0
+    return float(ts.item()), q.cpu().numpy(), sfa.cpu().numpy()
+
+
+def check_plain(h3, x, m_pad, ldx=None):
+    ts_o, q_o, sf_o, _ = oracle.plain_producer(x, m_pad)
+    ts, q, sfa = run_plain(h3, x, m_pad, ldx)
+    assert _f32_bits(ts) == _f32_bits(ts_o), (ts, ts_o)
+    assert np.array_equal(q, q_o), f"QDATA differs at {np.argwhere(q != q_o)[:5].tolist()}"
+    assert np.array_equal(sfa, oracle.swizzle_sf(sf_o))
+    return ts
+
+
+def test_plain_tiny_adversarial_bit_exact(h3):
+    """The adversarial tiny activation (outlier, midpoints, zero and tiny-scale
+    blocks, -0 rows, subnormals) packed as it is."""
+    from oracle.adversarial import tiny_adversarial
+    w = W.WORKLOADS["tiny"]
+    a = W.activations(w)
+    x = tiny_adversarial(_u16(a["x"]), _u16(a["shift"]), _u16(a["scale"]), W.seg_offsets(w))
+    check_plain(h3, x, w.m_pad)
+
+
+@pytest.mark.parametrize("m,m_pad,d,scale,ldx", [
+    (1, 16, 256, 1.0, None), (300, 320, 768, 7.0, None), (129, 256, 512, 0.01, 520), (1000, 1024, 7168, 3.0, None),
+])
+def test_plain_bit_exact(h3, m, m_pad, d, scale, ldx):
+    g = torch.Generator().manual_seed(m + d)
+    x = _bf16(torch.randn(m, d, generator=g) * scale)
+    x[0, :16] = 0x8000                      # a whole block of -0: scale 0, codes keep the sign
+    check_plain(h3, x, m_pad, ldx)
+
+
+def test_plain_zero_rows(h3):
+    ts, q, sfa = run_plain(h3, np.zeros((0, 256), dtype=np.uint16), 16)
+    assert ts == 0.0 and not q.any() and not sfa.any()
+
+
 def test_swizzle_kernel_matches_oracle_layout(h3):
     rng = np.random.default_rng(17)
     for rows, cols in [(384, 16), (300, 64), (1, 4), (129, 896)]:

@@ -366,6 +366,27 @@ def test_swiglu_is_rounded_product():
     assert np.array_equal(h, ref)
 
 
+def test_plain_producer_is_identity_modulation_except_negative_zero():
+    """Without a fused transform the producer packs x itself.  With shift = scale
+    = 0 the modulation is y = RN(RN(x * RN(0 + 1)) + 0) = x wherever x is not -0,
+    so both producers must give the same bytes there (the modulation producer is
+    pinned to torch's bf16 arithmetic above); at x = -0 the modulation's +0
+    shift gives +0 (E2M1 code 0x0) while the plain producer keeps the sign
+    (code 0x8)."""
+    g = torch.Generator().manual_seed(41)
+    x = (torch.randn(130, 512, generator=g) * 3).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    x[x == 0x8000] = 0
+    zero = np.zeros((1, 512), dtype=np.uint16)
+    ts_p, q_p, sf_p, _ = oracle.plain_producer(x, 144)
+    ts_m, q_m, sf_m, _, _ = oracle.modulate_producer(x, zero, zero, [0, 130], 144)
+    assert ts_p == ts_m and np.array_equal(q_p, q_m) and np.array_equal(sf_p, sf_m)
+    x[5, 17] = 0x8000                       # element 17: high nibble of byte 8 of row 5
+    _, q_p, _, _ = oracle.plain_producer(x, 144)
+    _, q_m, _, _, _ = oracle.modulate_producer(x, zero, zero, [0, 130], 144)
+    assert q_p[5, 8] >> 4 == 0x8 and q_m[5, 8] >> 4 == 0x0
+    assert np.array_equal(np.delete(q_p.ravel(), 5 * 256 + 8), np.delete(q_m.ravel(), 5 * 256 + 8))
+
+
 # ---------------------------------------------------------------------------
 # GEMM reference
 # ---------------------------------------------------------------------------
