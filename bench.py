@@ -180,8 +180,11 @@ def _bytes_per_element(kind):
     return (4 + 2 + 2 + 0.5 + 1 / 16) if kind == "swiglu" else (2 + 2 + 0.5 + 1 / 16)
 
 
+GATED = ("h3_attn", "h3_fc2")   # projections whose output enters the residual stream through a gate
+
+
 class Linear:
-    def __init__(self, h3, W, name, dev, gemm_kernel=0):
+    def __init__(self, h3, W, name, dev, gemm_kernel=0, gated=False):
         import torch
         self.h3, self.name = h3, name
         self.w = w = W.WORKLOADS[name]
@@ -203,6 +206,14 @@ class Linear:
         self.prod_bytes = _bytes_per_element(w.kind) * w.m * w.k
         self.launches = 3          # absmax kernel, pack kernel, GEMM kernel
         self.cfg = h3.GemmConfig(0, 0, gemm_kernel, 0) if gemm_kernel else None
+        # gated residual epilogue: out = RN(res + RN(gate_s * C)), gate per stream segment
+        self.gated = gated and name in GATED
+        if self.gated:
+            g = torch.Generator(device=dev)
+            g.manual_seed(w.seed + 200)
+            self.gate_off = [0, 32_768, w.m]
+            self.gate = torch.randn(2, w.n, generator=g, device=dev).to(torch.bfloat16).view(torch.int16)
+            self.res = (torch.randn(w.m, w.n, generator=g, device=dev) * 4).to(torch.bfloat16).view(torch.int16)
         self.ev = None
 
     def inputs(self):
@@ -222,7 +233,11 @@ class Linear:
                            scratch=self.scratch, qdata=self.q, sfa=self.sfa)
         if events is not None:
             events[1].record()
-        h3.gemm(self.q, self.sfa, self.ts, self.bq, self.bsf, self.bts, w.m, out=self.c, cfg=self.cfg)
+        if self.gated:
+            h3.gemm_gated_residual(self.q, self.sfa, self.ts, self.bq, self.bsf, self.bts, w.m, self.gate,
+                                   self.gate_off, self.res, out=self.c, cfg=self.cfg)
+        else:
+            h3.gemm(self.q, self.sfa, self.ts, self.bq, self.bsf, self.bts, w.m, out=self.c, cfg=self.cfg)
         if events is not None:
             events[2].record()
 
@@ -242,7 +257,7 @@ def run_ours(args, rank, world, local_rank):
     h3.lib()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    lins = [Linear(h3, W, n, dev, args.gemm_kernel) for n in LINEARS]
+    lins = [Linear(h3, W, n, dev, args.gemm_kernel, args.gated) for n in LINEARS]
     torch.cuda.synchronize()
 
     def step(ev=None):
@@ -321,6 +336,7 @@ def run_ours(args, rank, world, local_rank):
             "producer_ms": round(p["producer_ms"], 4), "producer_gbs": round(gbs, 1),
             "producer_hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
             "gemm_ms": round(p["gemm_ms"], 4), "gemm_tflops": round(tfl, 1),
+            "epilogue": "gated residual" if L.gated else "bf16",
             "gemm_fp4_frac": round(tfl / fp4_peak, 4)}
     dom = max(lins, key=lambda L: per[L.name]["gemm_ms"])
     dom_ms = per[dom.name]["gemm_ms"]
@@ -426,6 +442,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--widths", choices=sorted(WIDTHS), default="baseline",
                     help="linear set: the benchmark's configs (default) or the model's own projection widths")
+    ap.add_argument("--gated", action="store_true",
+                    help="--widths h3: attention output and FC2 use the gated residual epilogue")
     ap.add_argument("--gemm-kernel", type=int, default=0, choices=(0, 1, 2, 3),
                     help="GEMM kernel (h3fp4_gemm_config.cta_pair): 0 library default, 1 single CTA, "
                          "2 CTA pair, 3 two-CTA cluster with B multicast")

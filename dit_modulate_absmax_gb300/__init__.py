@@ -28,6 +28,8 @@ _SIGNATURES = {
     "h3fp4_modulate_pack": ([_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _I32, _P, _P, _P, _P], _STATUS),
     "h3fp4_swiglu_pack": ([_P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P], _STATUS),
     "h3fp4_quantize_pack": ([_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P], _STATUS),
+    "h3fp4_gemm_gated_residual": ([_P, _P, _P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I64, _P, _I64, _I64, _I64, _I64,
+                                   _I64, _P, _P], _STATUS),
     "h3fp4_gemm": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P], _STATUS),
     "h3fp4_swizzle_scales": ([_P, _I64, _I64, _I64, _P, _P], _STATUS),
     "h3fp4_swiglu_pack_noalloc": ([_P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P], _STATUS),
@@ -114,6 +116,13 @@ def h3fp4_quantize_pack(x, ldx, m, m_pad, d, tensor_scale, scratch, qdata, sfa, 
 def h3fp4_gemm(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg: GemmConfig | None = None, stream=0):
     _call("h3fp4_gemm", a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k,
           ctypes.byref(cfg) if cfg is not None else None, stream)
+
+
+def h3fp4_gemm_gated_residual(a_q, a_sf, a_ts, b_q, b_sf, b_ts, gate, ld_gate, seg_row_offsets, residual, ldr, out,
+                              ldo, m, m_pad, n, k, cfg: GemmConfig | None = None, stream=0):
+    offs, nseg = _offsets(seg_row_offsets)
+    _call("h3fp4_gemm_gated_residual", a_q, a_sf, a_ts, b_q, b_sf, b_ts, gate, ld_gate, offs, nseg, residual, ldr,
+          out, ldo, m, m_pad, n, k, ctypes.byref(cfg) if cfg is not None else None, stream)
 
 
 def h3fp4_swizzle_scales(sf_logical, rows, cols, ld, sf_out, stream=0):
@@ -239,6 +248,23 @@ def gemm(a_q, a_sf, a_ts, b_q, b_sf, b_ts, m, *, out=None, cfg: GemmConfig | Non
         out = torch.empty(m, n, dtype=torch.int16, device=a_q.device)
     h3fp4_gemm(a_q.data_ptr(), a_sf.data_ptr(), a_ts.data_ptr(), b_q.data_ptr(), b_sf.data_ptr(), b_ts.data_ptr(),
                out.data_ptr(), out.stride(0), m, m_pad, n, 2 * kh, cfg, _stream(stream))
+    return out
+
+
+def gemm_gated_residual(a_q, a_sf, a_ts, b_q, b_sf, b_ts, m, gate, seg_row_offsets, residual, *, out=None,
+                       cfg: GemmConfig | None = None, stream=None):
+    """out = RN_bf16(residual + RN_bf16(gate_s * C)) with C the GEMM result; pass
+    out=residual to update the residual in place.  Returns out (int16 bf16 patterns)."""
+    import torch
+    _need_cuda(a_q, a_sf, a_ts, b_q, b_sf, b_ts, gate, residual, out)
+    m_pad, kh = a_q.shape
+    n = b_q.shape[0]
+    if out is None:
+        out = torch.empty(m, n, dtype=torch.int16, device=a_q.device)
+    h3fp4_gemm_gated_residual(a_q.data_ptr(), a_sf.data_ptr(), a_ts.data_ptr(), b_q.data_ptr(), b_sf.data_ptr(),
+                              b_ts.data_ptr(), gate.data_ptr(), gate.stride(0), seg_row_offsets,
+                              residual.data_ptr(), residual.stride(0), out.data_ptr(), out.stride(0), m, m_pad, n,
+                              2 * kh, cfg, _stream(stream))
     return out
 
 

@@ -147,9 +147,12 @@ h3fp4_status h3fp4_quantize_pack(const void *x_bf16, int64_t ldx, int64_t m, int
                                                  tensor_scale, scratch, qdata, sfa, as_stream(stream)));
 }
 
-h3fp4_status h3fp4_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_tensor_scale, const uint8_t *b_q,
-                        const uint8_t *b_sf, const float *b_tensor_scale, void *c_bf16, int64_t ldc, int64_t m,
-                        int64_t m_pad, int64_t n, int64_t k, const h3fp4_gemm_config *cfg, void *stream)
+namespace {
+
+// Checks shared by both GEMM entry points; fills `c` with the configuration.
+h3fp4_status check_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_tensor_scale, const uint8_t *b_q,
+                        const uint8_t *b_sf, const float *b_tensor_scale, const void *c_bf16, int64_t ldc, int64_t m,
+                        int64_t m_pad, int64_t n, int64_t k, const h3fp4_gemm_config *cfg, h3fp4_gemm_config *c)
 {
     if (a_q == nullptr || a_sf == nullptr || a_tensor_scale == nullptr || b_q == nullptr || b_sf == nullptr ||
         b_tensor_scale == nullptr || (c_bf16 == nullptr && m != 0 && n != 0))
@@ -160,14 +163,63 @@ h3fp4_status h3fp4_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_
     if (!aligned16(a_q) || !aligned16(a_sf) || !aligned16(b_q) || !aligned16(b_sf) || !aligned16(c_bf16) ||
         ldc % 8 != 0)
         return H3FP4_ERR_ALIGN;
-    h3fp4_gemm_config c = {0, 0, 0, 0};
+    *c = h3fp4_gemm_config{0, 0, 0, 0};
     if (cfg != nullptr) {
-        c = *cfg;
-        if (c.n_group < 0 || c.stages != 0 || c.cta_pair < 0 || c.cta_pair > 3 || c.reserved != 0)
+        *c = *cfg;
+        if (c->n_group < 0 || c->stages != 0 || c->cta_pair < 0 || c->cta_pair > 3 || c->reserved != 0)
             return H3FP4_ERR_UNSUPPORTED;
     }
+    return H3FP4_OK;
+}
+
+}  // namespace
+
+h3fp4_status h3fp4_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_tensor_scale, const uint8_t *b_q,
+                        const uint8_t *b_sf, const float *b_tensor_scale, void *c_bf16, int64_t ldc, int64_t m,
+                        int64_t m_pad, int64_t n, int64_t k, const h3fp4_gemm_config *cfg, void *stream)
+{
+    h3fp4_gemm_config c;
+    h3fp4_status s = check_gemm(a_q, a_sf, a_tensor_scale, b_q, b_sf, b_tensor_scale, c_bf16, ldc, m, m_pad, n, k, cfg, &c);
+    if (s != H3FP4_OK)
+        return s;
     return h3fp4::launch_gemm(a_q, a_sf, a_tensor_scale, b_q, b_sf, b_tensor_scale,
-                              static_cast<uint16_t *>(c_bf16), ldc, m, m_pad, n, k, c, as_stream(stream));
+                              static_cast<uint16_t *>(c_bf16), ldc, m, m_pad, n, k, c, nullptr, as_stream(stream));
+}
+
+h3fp4_status h3fp4_gemm_gated_residual(const uint8_t *a_q, const uint8_t *a_sf, const float *a_tensor_scale,
+                                       const uint8_t *b_q, const uint8_t *b_sf, const float *b_tensor_scale,
+                                       const void *gate_bf16, int64_t ld_gate, const int32_t *seg_row_offsets,
+                                       int32_t nseg, const void *residual_bf16, int64_t ldr, void *out_bf16,
+                                       int64_t ldo, int64_t m, int64_t m_pad, int64_t n, int64_t k,
+                                       const h3fp4_gemm_config *cfg, void *stream)
+{
+    h3fp4_gemm_config c;
+    h3fp4_status s = check_gemm(a_q, a_sf, a_tensor_scale, b_q, b_sf, b_tensor_scale, out_bf16, ldo, m, m_pad, n, k,
+                                cfg, &c);
+    if (s != H3FP4_OK)
+        return s;
+    const bool rows = m != 0 && n != 0;
+    if (rows && (gate_bf16 == nullptr || residual_bf16 == nullptr))
+        return H3FP4_ERR_NULL;
+    if (ld_gate < n || ldr < n)
+        return H3FP4_ERR_SHAPE;
+    if (!aligned16(gate_bf16) || !aligned16(residual_bf16) || ld_gate % 8 != 0 || ldr % 8 != 0)
+        return H3FP4_ERR_ALIGN;
+    SegTable seg;
+    if ((s = make_segments(seg_row_offsets, nseg, m, &seg)) != H3FP4_OK)
+        return s;
+    if (rows) {   // the output either is the residual (same leading dimension) or does not overlap it
+        const char *o = static_cast<const char *>(out_bf16), *r = static_cast<const char *>(residual_bf16);
+        const int64_t ob = ((m - 1) * ldo + n) * 2, rb = ((m - 1) * ldr + n) * 2;
+        const bool same = o == r && ldo == ldr;
+        if (!same && o < r + rb && r < o + ob)
+            return H3FP4_ERR_UNSUPPORTED;
+    }
+    if (c.cta_pair == 2)
+        return H3FP4_ERR_UNSUPPORTED;
+    h3fp4::GatedArgs g{static_cast<const uint16_t *>(gate_bf16), ld_gate, seg, residual_bf16, ldr};
+    return h3fp4::launch_gemm(a_q, a_sf, a_tensor_scale, b_q, b_sf, b_tensor_scale, static_cast<uint16_t *>(out_bf16),
+                              ldo, m, m_pad, n, k, c, &g, as_stream(stream));
 }
 
 h3fp4_status h3fp4_swizzle_scales(const uint8_t *sf_logical, int64_t rows, int64_t cols, int64_t ld,

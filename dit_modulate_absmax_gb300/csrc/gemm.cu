@@ -94,6 +94,7 @@ struct __align__(1024) Smem {
     uint8_t sfa[kStages][SFA_BYTES];
     uint8_t sfb[kStages][SFB_BYTES];
     uint8_t cst[kEpiWarps][CST_BYTES];  // per epilogue warp: output staging for tensor stores
+    uint64_t res_full[kEpiWarps];       // per epilogue warp: a residual block landed in cst (gated epilogue)
     uint64_t full[kStages];      // A and B tiles landed
     uint64_t sf_full[kStages];   // scale atoms landed
     uint64_t empty[kStages];
@@ -193,6 +194,98 @@ __device__ __forceinline__ void store_rows(const CUtensorMap *tmC, uint32_t buf,
     }
 }
 
+// Arguments of the gated residual epilogue: gate [nseg, n] bf16 (leading
+// dimension ld_gate) selected per output row by the row segments off[0..nseg].
+struct GatedEpilogue {
+    const uint16_t *gate;
+    int64_t ld_gate;
+    int32_t off[H3FP4_MAX_SEGMENTS + 1];
+    int32_t nseg;
+};
+
+// Segment of row r: the number of interior boundaries off[1..nseg-1] at or
+// below r (fully unrolled, constant indices, so the table stays in
+// kernel-parameter space).
+__device__ __forceinline__ const uint16_t *gate_row(const GatedEpilogue &ge, int r)
+{
+    int s = 0;
+#pragma unroll
+    for (int i = 1; i < H3FP4_MAX_SEGMENTS; ++i)
+        s += (i < ge.nseg && r >= ge.off[i]) ? 1 : 0;
+    return ge.gate + static_cast<int64_t>(s) * ge.ld_gate;
+}
+
+__device__ __forceinline__ uint32_t bf2_mul_rn(uint32_t a, uint32_t b)
+{
+    __nv_bfloat162 x, y;
+    memcpy(&x, &a, 4);
+    memcpy(&y, &b, 4);
+    const __nv_bfloat162 r = __hmul2_rn(x, y);
+    uint32_t u;
+    memcpy(&u, &r, 4);
+    return u;
+}
+
+__device__ __forceinline__ uint32_t bf2_add_rn(uint32_t a, uint32_t b)
+{
+    __nv_bfloat162 x, y;
+    memcpy(&x, &a, 4);
+    memcpy(&y, &b, 4);
+    const __nv_bfloat162 r = __hadd2_rn(x, y);
+    uint32_t u;
+    memcpy(&u, &r, 4);
+    return u;
+}
+
+// Gated residual form of store_rows ("NVFP4 Streaming Design", P4: the
+// explicit BF16 conversion, gate multiply, residual add and final BF16
+// rounding): out = RN_bf16(res + RN_bf16(gate * c)) with c the BF16 GEMM
+// result held in pk.  Per 16-column block the warp loads its 32 x 16
+// residual block into its buffer with a tensor copy (rows past the tensor
+// map's M extent read as zero), combines it in registers with correctly
+// rounded bf16x2 multiply and add, writes the result back into the buffer and
+// stores it with a tensor store.  `res` may be the output itself: each block
+// is read before it is written, by the same warp.
+__device__ __forceinline__ bool store_rows_gated(const CUtensorMap *tmC, const CUtensorMap *tmR, uint32_t buf,
+                                                 uint32_t bar, uint32_t &phase, const uint32_t (&pk)[64], int col0,
+                                                 int row0, int lane, const uint16_t *grow)
+{
+#pragma unroll   // constant indices into pk keep it in registers
+    for (int c = 0; c < 128 / CST_COLS; ++c) {
+        if (lane == 0) {
+            bulk_wait_group_read0();   // the previous store has finished reading the buffer
+            mbar_arrive_expect_tx(bar, CST_BYTES);
+            tma_load_2d(buf, tmR, col0 + c * CST_COLS, row0, bar);
+        }
+        __syncwarp();
+        // every lane waits on the barrier (the residual block written by the copy engine)
+        if (!warp_wait(bar, phase))
+            return false;
+        phase ^= 1u;
+        const uint4 r0 = ld_shared_v4(buf + lane * 32);
+        const uint4 r1 = ld_shared_v4(buf + lane * 32 + 16);
+        const uint4 g0 = *reinterpret_cast<const uint4 *>(grow + col0 + c * CST_COLS);
+        const uint4 g1 = *reinterpret_cast<const uint4 *>(grow + col0 + c * CST_COLS + 8);
+        const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        uint32_t o[8];
+        const int w = c * (CST_COLS / 2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            o[i] = bf2_add_rn(rw[i], bf2_mul_rn(gw[i], pk[w + i]));
+        __syncwarp();   // every lane has read the residual before any lane overwrites the buffer
+        st_shared_v4(buf + lane * 32, o[0], o[1], o[2], o[3]);
+        st_shared_v4(buf + lane * 32 + 16, o[4], o[5], o[6], o[7]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, buf, col0 + c * CST_COLS, row0);
+            bulk_commit_group();
+        }
+    }
+    return true;
+}
+
 // Output tile t of the persistent schedule: groups of n_group N-tiles x all
 // M-tiles, N fastest inside a group (the last group may be narrower).
 __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int n_group, int &mt, int &nt)
@@ -217,10 +310,11 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
 // cluster may hold an M tile past the last one when the M tile count is odd:
 // its A rows read as zero, its A scales are not loaded and its output rows are
 // clipped by the tensor stores.
-template <bool kMcast>
+template <bool kMcast, bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const uint8_t *__restrict__ a_sf,
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
+                     const __grid_constant__ GatedEpilogue ge, const uint8_t *__restrict__ a_sf,
                      const uint8_t *__restrict__ b_sf, const float *__restrict__ a_ts,
                      const float *__restrict__ b_ts, int m, int n, int k, int m_tiles, int n_tiles, int n_group)
 {
@@ -251,10 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(&sm.acc_full), 1);
         mbar_init(smem_u32(&sm.acc_empty), kEpiWarps);
+        for (int w = 0; w < kEpiWarps; ++w)
+            mbar_init(smem_u32(&sm.res_full[w]), 1);
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmC);
+        if (kGated)
+            prefetch_tmap(&tmR);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
@@ -385,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                          // TMEM lane quarter this warp may access
         const int half = (warp - kFirstEpiWarp) >> 2;    // which 128 accumulator columns it drains
         const float alpha = __fmul_rn(*a_ts, *b_ts);
-        uint32_t local = 0;
+        uint32_t local = 0, rphase = 0;
         for (int t = sched_first; t < total_tiles; t += sched_step, ++local) {
             int mt, nt;
             coords(t, mt, nt);
@@ -421,8 +519,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&sm.acc_empty));   // accumulator free for the next tile
-            store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpiWarp]), pk, nt * BN + half * 128, mt * BM + q * 32,
-                       lane);
+            if (kGated) {
+                const int row0 = mt * BM + q * 32;
+                if (!store_rows_gated(&tmC, &tmR, smem_u32(sm.cst[warp - kFirstEpiWarp]),
+                                      smem_u32(&sm.res_full[warp - kFirstEpiWarp]), rphase, pk, nt * BN + half * 128,
+                                      row0, lane, gate_row(ge, row0 + lane))) {
+                    if (lane == 0)
+                        record_error(ERR_WAIT_ACC);
+                    break;
+                }
+            } else {
+                store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpiWarp]), pk, nt * BN + half * 128, mt * BM + q * 32,
+                           lane);
+            }
         }
         if (lane == 0)
             bulk_wait_group0();
@@ -832,43 +941,37 @@ h3fp4_status launch_pair(const uint8_t *a_q, const uint8_t *a_sf, const float *a
 
 }  // namespace
 
-h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
-                         const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m, int64_t m_pad,
-                         int64_t n, int64_t k, const h3fp4_gemm_config &cfg, cudaStream_t st)
+namespace {
+
+template <bool kMcast, bool kGated>
+h3fp4_status launch_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const CUtensorMap &tmR,
+                          const GatedEpilogue &ge, const uint8_t *a_sf, const uint8_t *b_sf, const float *a_ts,
+                          const float *b_ts, int64_t m, int64_t n, int64_t k, int n_group_cfg, cudaStream_t st)
 {
-    if (m == 0 || n == 0)
-        return H3FP4_OK;
-    if (cfg.cta_pair == 2)
-        return launch_pair(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, st);
-    const bool mcast = cfg.cta_pair == 3 || cfg.cta_pair == 0;   // the default: measured fastest in the DiT step
-    CUtensorMap tmA, tmB, tmC;
-    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, BM) ||
-        !make_operand_map(&tmB, b_q, n, k / 2, mcast ? BN / 2 : BN) || !make_output_map(&tmC, c, m, n, ldc))
-        return H3FP4_ERR_CUDA;
-    static bool attr_set[2][64] = {{false}};
+    static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return H3FP4_ERR_CUDA;
-    if (dev >= 0 && dev < 64 && !attr_set[mcast][dev]) {
-        if (cudaFuncSetAttribute(mcast ? nvf4_gemm_kernel<true> : nvf4_gemm_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) != cudaSuccess)
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(nvf4_gemm_kernel<kMcast, kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes)) != cudaSuccess)
             return H3FP4_ERR_CUDA;
-        attr_set[mcast][dev] = true;
+        attr_set[dev] = true;
     }
     const int m_tiles = static_cast<int>((m + BM - 1) / BM);
     const int n_tiles = static_cast<int>((n + BN - 1) / BN);
-    const int m_sched = mcast ? (m_tiles + 1) / 2 : m_tiles;
+    const int m_sched = kMcast ? (m_tiles + 1) / 2 : m_tiles;
     const int64_t total = static_cast<int64_t>(m_sched) * n_tiles;
     if (total > 0x7FFFFFFF)
         return H3FP4_ERR_SHAPE;
-    int n_group = cfg.n_group > 0 ? cfg.n_group : kDefaultNGroup;
+    int n_group = n_group_cfg > 0 ? n_group_cfg : kDefaultNGroup;
     if (n_group > n_tiles)
         n_group = n_tiles;
-    if (!mcast) {
+    if (!kMcast) {
         const int grid = static_cast<int>(total < sm_count() ? total : sm_count());
-        nvf4_gemm_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, tmC, a_sf, b_sf, a_ts, b_ts,
-                                                                   static_cast<int>(m), static_cast<int>(n),
-                                                                   static_cast<int>(k), m_tiles, n_tiles, n_group);
+        nvf4_gemm_kernel<false, kGated><<<grid, kThreads, kSmemBytes, st>>>(
+            tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, static_cast<int>(m), static_cast<int>(n),
+            static_cast<int>(k), m_tiles, n_tiles, n_group);
         return cudaGetLastError() == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
     }
     const int max_clusters = sm_count() / 2;
@@ -885,10 +988,47 @@ h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&lc, nvf4_gemm_kernel<true>, tmA, tmB, tmC, a_sf, b_sf, a_ts, b_ts,
-                                             static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), m_tiles,
-                                             n_tiles, n_group);
+    const cudaError_t e = cudaLaunchKernelEx(&lc, nvf4_gemm_kernel<true, kGated>, tmA, tmB, tmC, tmR, ge, a_sf, b_sf,
+                                             a_ts, b_ts, static_cast<int>(m), static_cast<int>(n),
+                                             static_cast<int>(k), m_tiles, n_tiles, n_group);
     return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
+}
+
+}  // namespace
+
+h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
+                         const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m, int64_t m_pad,
+                         int64_t n, int64_t k, const h3fp4_gemm_config &cfg, const GatedArgs *gated, cudaStream_t st)
+{
+    if (m == 0 || n == 0)
+        return H3FP4_OK;
+    if (cfg.cta_pair == 2) {
+        if (gated != nullptr)
+            return H3FP4_ERR_UNSUPPORTED;
+        return launch_pair(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, st);
+    }
+    const bool mcast = cfg.cta_pair == 3 || cfg.cta_pair == 0;   // the default: measured fastest in the DiT step
+    CUtensorMap tmA, tmB, tmC, tmR;
+    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, BM) ||
+        !make_operand_map(&tmB, b_q, n, k / 2, mcast ? BN / 2 : BN) || !make_output_map(&tmC, c, m, n, ldc))
+        return H3FP4_ERR_CUDA;
+    GatedEpilogue ge{};
+    if (gated != nullptr) {
+        if (!make_output_map(&tmR, const_cast<void *>(gated->residual), m, n, gated->ldr))
+            return H3FP4_ERR_CUDA;
+        ge.gate = gated->gate;
+        ge.ld_gate = gated->ld_gate;
+        for (int i = 0; i <= H3FP4_MAX_SEGMENTS; ++i)
+            ge.off[i] = gated->seg.off[i];
+        ge.nseg = gated->seg.nseg;
+    } else {
+        tmR = tmC;   // unused
+    }
+    if (mcast)
+        return gated ? launch_tiles<true, true>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st)
+                     : launch_tiles<true, false>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st);
+    return gated ? launch_tiles<false, true>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st)
+                 : launch_tiles<false, false>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st);
 }
 
 h3fp4_status read_device_error(uint32_t *code)

@@ -36,9 +36,20 @@ cudaError_t launch_quantize_pack(const uint16_t *x, int64_t ldx, int64_t m, int6
 cudaError_t launch_swizzle_scales(const uint8_t *src, int64_t rows, int64_t cols, int64_t ld,
                                   uint8_t *dst, cudaStream_t st);
 
+// Gated residual epilogue of the GEMM: out = RN_bf16(residual + RN_bf16(gate_s * c)),
+// gate [nseg, n] bf16 selected by the row segments.
+struct GatedArgs {
+    const uint16_t *gate;
+    int64_t ld_gate;
+    SegTable seg;
+    const void *residual;
+    int64_t ldr;
+};
+
 h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
                          const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m,
-                         int64_t m_pad, int64_t n, int64_t k, const h3fp4_gemm_config &cfg, cudaStream_t st);
+                         int64_t m_pad, int64_t n, int64_t k, const h3fp4_gemm_config &cfg, const GatedArgs *gated,
+                         cudaStream_t st);
 
 h3fp4_status read_device_error(uint32_t *code);
 

@@ -205,6 +205,31 @@ H3FP4_API h3fp4_status h3fp4_gemm(const uint8_t *a_q, const uint8_t *a_sf, const
                         const h3fp4_gemm_config *cfg, void *stream);
 
 /*
+ * h3fp4_gemm_gated_residual -- h3fp4_gemm with the gated residual epilogue.
+ * Source: "NVFP4 Streaming Design", P4: Exact Epilogue (after the owned GEMM,
+ * the explicit BF16 conversion, gate multiply, residual add and final BF16
+ * rounding sequence), for the projections whose output is added to the
+ * residual stream through an AdaLN gate (attention output, FC2).
+ *
+ * out[i, j] = RN_bf16(residual[i, j] + RN_bf16(gate[s(i), j] * c[i, j]))
+ * with c[i, j] the value h3fp4_gemm would write and s(i) the segment of row i
+ * (seg_row_offsets as for h3fp4_modulate_absmax: host array of nseg + 1
+ * non-decreasing offsets, [0] = 0, [nseg] = m).  Only rows i < m and columns
+ * j < n are written.
+ *
+ *   gate_bf16      [nseg, n] bf16, leading dimension ld_gate (>= n, multiple of 8), 16-byte aligned
+ *   residual_bf16  [m, n] bf16, leading dimension ldr (>= n, multiple of 8), 16-byte aligned
+ *   out_bf16       [m, n] bf16, leading dimension ldo; either the residual itself (same pointer and
+ *                  leading dimension: updated in place) or not overlapping it (else H3FP4_ERR_UNSUPPORTED)
+ *   other arguments as for h3fp4_gemm; cfg->cta_pair = 2 is not supported (H3FP4_ERR_UNSUPPORTED)
+ */
+H3FP4_API h3fp4_status h3fp4_gemm_gated_residual(
+    const uint8_t *a_q, const uint8_t *a_sf, const float *a_tensor_scale, const uint8_t *b_q, const uint8_t *b_sf,
+    const float *b_tensor_scale, const void *gate_bf16, int64_t ld_gate, const int32_t *seg_row_offsets, int32_t nseg,
+    const void *residual_bf16, int64_t ldr, void *out_bf16, int64_t ldo, int64_t m, int64_t m_pad, int64_t n,
+    int64_t k, const h3fp4_gemm_config *cfg, void *stream);
+
+/*
  * h3fp4_swizzle_scales -- helper for preparing weights: copies a LOGICAL
  * row-major E4M3 scale matrix [rows, cols] (leading dimension ld bytes) into
  * the scale layout above, padding rows up to a multiple of 128 with zeros.

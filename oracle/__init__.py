@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
     L.orc_e2m1_encode.argtypes = [ctypes.c_double]
     L.orc_modulate.restype = None
     L.orc_modulate.argtypes = [_P, _I64, _I64, _I64, _P, _P, _I64, _P, ctypes.c_int32, _P, _I64]
+    L.orc_gated_residual.restype = None
+    L.orc_gated_residual.argtypes = [_P, _I64, _P, _I64, _P, ctypes.c_int32, _P, _I64, _I64, _I64, _P, _I64]
     L.orc_swiglu.restype = None
     L.orc_swiglu.argtypes = [_P, _I64, _P, _I64, _I64, _I64, _P, _P, _I64]
     L.orc_absmax.restype = ctypes.c_uint16
@@ -375,6 +377,54 @@ def gemm_reference(qa, sfa, ts_a, qb, sfb, ts_b, k: int, rows=None, n_chunk: int
         R[:, n0:n1] = A @ B.T
         S[:, n0:n1] = Aabs @ np.abs(B).T
     return R, S
+
+
+def gated_residual(c, gate, seg_off, res) -> np.ndarray:
+    """out = RN_bf16(res + RN_bf16(gate_s * c)) per element, gate_s the gate row of
+    the row's segment ("NVFP4 Streaming Design", P4).  c, res: uint16 [m, n];
+    gate: uint16 [nseg, n]; seg_off: nseg + 1 row offsets (0 ... m)."""
+    c, gate, res = _u16(c), _u16(gate), _u16(res)
+    m, n = c.shape
+    off = np.ascontiguousarray(np.asarray(seg_off, dtype=np.int32))
+    nseg = len(off) - 1
+    assert gate.shape == (nseg, n) and res.shape == (m, n)
+    assert off[0] == 0 and off[-1] == m and np.all(np.diff(off) >= 0)
+    out = np.empty((m, n), dtype=np.uint16)
+    lib().orc_gated_residual(_ptr(c), n, _ptr(gate), n, _ptr(off), nseg, _ptr(res), n, m, n, _ptr(out), n)
+    return out
+
+
+def _bf16_directed(v: np.ndarray, up: bool) -> np.ndarray:
+    """bf16 bit patterns of the smallest bf16 >= v (up) or the largest <= v,
+    for finite v inside the bf16 range (no overflow handling needed here)."""
+    v = np.asarray(v, dtype=np.float64)
+    bits = np.array([bf16_bits(float(x)) for x in v.ravel()], dtype=np.int64).reshape(v.shape)
+    vals = bf16_to_f64(bits.astype(np.uint16))
+    need = (vals < v) if up else (vals > v)
+    # one bf16 step in the needed direction: on the bit pattern, +1 moves away
+    # from zero and -1 towards it; from +-0 the step goes to the smallest
+    # subnormal of the needed sign
+    pos, neg = vals > 0, vals < 0
+    if up:
+        step = np.where(pos, bits + 1, np.where(neg, bits - 1, 0x0001))
+    else:
+        step = np.where(pos, bits - 1, np.where(neg, bits + 1, 0x8001))
+    return np.where(need, step, bits).astype(np.uint16)
+
+
+def gated_residual_bounds(R, S, gate, seg_off, res):
+    """Every output the gated epilogue may give for a GEMM result within the
+    GEMM tolerance of R: with c ranging over the bf16 values in
+    [R - tol, R + tol] (tol as in gemm_tolerance), out(c) = RN(res + RN(g c))
+    is monotone in c (non-decreasing for g >= 0, non-increasing for g < 0), so
+    the outputs lie between out(c_lo) and out(c_hi).  Returns (lo, hi) as
+    float64 arrays."""
+    tol = gemm_tolerance(R, S)
+    c_lo = _bf16_directed(R - tol, up=True)
+    c_hi = _bf16_directed(R + tol, up=False)
+    o1 = bf16_to_f64(gated_residual(c_lo, gate, seg_off, res))
+    o2 = bf16_to_f64(gated_residual(c_hi, gate, seg_off, res))
+    return np.minimum(o1, o2), np.maximum(o1, o2)
 
 
 def ulp_bf16(v: np.ndarray) -> np.ndarray:

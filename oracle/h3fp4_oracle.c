@@ -176,6 +176,34 @@ void orc_modulate(const uint16_t *x, int64_t ldx, int64_t m, int64_t d,
 }
 
 /* ---------------------------------------------------------------------------
+ * Gated residual epilogue, "NVFP4 Streaming Design", P4 (exact epilogue):
+ * after the GEMM's BF16 conversion c, the gate multiply and the residual add,
+ * each rounded to BF16:
+ *   p = RN_bf16(gate_s * c);  out = RN_bf16(res + p)
+ * with gate_s the gate row of the row's segment.  A product of two bf16
+ * values is exact in double; a sum of two bf16 values is rounded to double
+ * only when their exponents differ by more than 45, where that rounding
+ * cannot move the bf16 result (53 >= 2 * 8 + 2).
+ * ------------------------------------------------------------------------- */
+void orc_gated_residual(const uint16_t *c, int64_t ldc, const uint16_t *gate, int64_t ld_gate,
+                        const int32_t *seg_off, int32_t nseg, const uint16_t *res, int64_t ldr,
+                        int64_t m, int64_t n, uint16_t *out, int64_t ldo)
+{
+    for (int64_t r = 0; r < m; ++r) {
+        int32_t s = 0;
+        while (s + 1 < nseg && r >= seg_off[s + 1])
+            ++s;
+        for (int64_t j = 0; j < n; ++j) {
+            double cv = orc_bf16_value(c[r * ldc + j]);
+            double g = orc_bf16_value(gate[s * ld_gate + j]);
+            double p = orc_rn_bf16(g * cv);
+            double rv = orc_bf16_value(res[r * ldr + j]);
+            out[r * ldo + j] = orc_bf16_bits(orc_rn_bf16(rv + p));
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------
  * SwiGLU producer input, "FC2 NVFP4 Library Scheduling", Exact Operation:
  *   h = RN_bf16(silu_bf16(gate) * up)
  * silu_table[g] is the bf16 pattern of the correctly rounded silu of the bf16

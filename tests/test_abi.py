@@ -128,6 +128,24 @@ def test_gemm_validation(L):
     assert call(cfg=ctypes.byref(bad)) == UNSUP
 
 
+def test_gemm_gated_residual_validation(L):
+    f = L.h3fp4_gemm_gated_residual
+    offs = (ctypes.c_int32 * 3)(0, 200, 300)
+
+    def call(gate=F, ld_gate=384, residual=F + 4096 * 1024, ldr=384, out=F, ldo=384, nseg=2, off=offs, cfg=None):
+        return f(F, F, F, F, F, F, gate, ld_gate, off, nseg, residual, ldr, out, ldo, 300, 320, 384, 256, cfg, None)
+
+    assert call(gate=None) == NULL
+    assert call(residual=None) == NULL
+    assert call(ld_gate=256) == SHAPE
+    assert call(ldr=256) == SHAPE
+    assert call(gate=F + 2) == ALIGN
+    assert call(ldr=388) == ALIGN
+    assert call(off=(ctypes.c_int32 * 3)(0, 250, 200)) == SHAPE          # offsets must not decrease
+    assert call(residual=F + 64) == UNSUP                                 # partial overlap with the output
+    assert call(cfg=ctypes.byref(pkg.GemmConfig(0, 0, 2, 0))) == UNSUP     # the pair kernel has no gated form
+
+
 def test_swizzle_and_device_error_validation(L):
     assert L.h3fp4_swizzle_scales(None, 10, 16, 16, F, None) == NULL
     assert L.h3fp4_swizzle_scales(F, 10, 6, 16, F, None) == SHAPE

@@ -162,3 +162,93 @@ def test_scale_atom_rows_are_not_mixed(h3, cfg):
     nz = np.argwhere(R != 0)
     assert set(map(int, np.unique(nz[:, 0]))) <= {0, 37, 95, 130, 255}
     check_tolerance(C, R, S)
+
+
+# ---------------------------------------------------------------------------
+# Gated residual epilogue ("NVFP4 Streaming Design", P4)
+# ---------------------------------------------------------------------------
+GATED_KERNELS = {"single": 1, "mcast": 3}
+
+
+def _gated_inputs(rng, m, n, nseg):
+    gate = torch.randn(nseg, n, generator=torch.Generator().manual_seed(int(rng.integers(1 << 30))))
+    res = torch.randn(m, n, generator=torch.Generator().manual_seed(int(rng.integers(1 << 30)))) * 4
+    return (gate.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16),
+            res.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+
+
+def run_gated(h3, qa, sfa, ts_a, qb, sfb, ts_b, m, gate, off, res, cfg, in_place=False, extra_rows=3):
+    m_pad, kh = qa.shape
+    n = qb.shape[0]
+    dev = "cuda"
+    a = torch.from_numpy(qa).to(dev)
+    asf = h3.swizzle_scales(torch.from_numpy(sfa).to(dev))
+    b = torch.from_numpy(qb).to(dev)
+    bsf = h3.swizzle_scales(torch.from_numpy(sfb).to(dev))
+    ta = torch.tensor([ts_a], dtype=torch.float32, device=dev)
+    tb = torch.tensor([ts_b], dtype=torch.float32, device=dev)
+    g = torch.from_numpy(gate.view(np.int16)).to(dev)
+    buf = torch.full((m + extra_rows, n), CANARY16, dtype=torch.int16, device=dev)
+    r = buf[:m]
+    r.copy_(torch.from_numpy(res.view(np.int16)))
+    if in_place:
+        h3.gemm_gated_residual(a, asf, ta, b, bsf, tb, m, g, off, r, out=r, cfg=cfg)
+        out = buf
+    else:
+        out = torch.full((m + extra_rows, n), CANARY16, dtype=torch.int16, device=dev)
+        h3.gemm_gated_residual(a, asf, ta, b, bsf, tb, m, g, off, r, out=out[:m], cfg=cfg)
+    torch.cuda.synchronize()
+    assert h3.h3fp4_device_error() == 0
+    o = out.cpu().numpy().view(np.uint16)
+    assert (o[m:] == CANARY16).all(), "rows >= m must not be written"
+    if not in_place:
+        assert np.array_equal(buf[:m].cpu().numpy().view(np.uint16), res), "the residual must not change"
+    return o[:m]
+
+
+@pytest.fixture(params=sorted(GATED_KERNELS), ids=sorted(GATED_KERNELS))
+def gcfg(request, h3):
+    return h3.GemmConfig(0, 0, GATED_KERNELS[request.param], 0)
+
+
+def test_gated_exact_products_bit_exact(h3, gcfg):
+    """Power-of-two scales make the GEMM result exact (c = RN_bf16(R)), so the
+    whole epilogue is determined: out must equal the oracle bit for bit."""
+    rng = np.random.default_rng(50)
+    m, m_pad, n, k = 300, 320, 384, 512
+    pow2 = np.array([0x28, 0x30, 0x38], dtype=np.uint8)
+    qa = rng.integers(0, 256, size=(m_pad, k // 2), dtype=np.uint8)
+    qa[m:] = 0
+    qb = rng.integers(0, 256, size=(n, k // 2), dtype=np.uint8)
+    sfa = np.zeros((384, k // 16), dtype=np.uint8)
+    sfb = np.zeros((384, k // 16), dtype=np.uint8)
+    sfa[:m] = rng.choice(pow2, size=(m, k // 16))
+    sfb[:n] = rng.choice(pow2, size=(n, k // 16))
+    off = [0, 200, 300]                      # a segment boundary inside the second M tile
+    gate, res = _gated_inputs(rng, m, n, 2)
+    got = run_gated(h3, qa, sfa, 0.125, qb, sfb, 4.0, m, gate, off, res, gcfg)
+    R, _ = oracle.gemm_reference(qa, sfa, 0.125, qb, sfb, 4.0, k, rows=np.arange(m))
+    c = np.vectorize(oracle.bf16_bits)(R).astype(np.uint16)
+    want = oracle.gated_residual(c, gate, off, res)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:4].tolist()}"
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+@pytest.mark.parametrize("m,m_pad,n,k,off", [
+    (130, 144, 256, 768, [0, 130]),
+    (513, 528, 640, 1024, [0, 100, 100, 513]),      # an empty segment
+])
+def test_gated_random_within_tolerance_bounds(h3, gcfg, m, m_pad, n, k, off, in_place):
+    rng = np.random.default_rng(m + n + k)
+    qa, sfa = _rand_operand(rng, m_pad, k, 0x28, 0x50)
+    qa[m:] = 0
+    sfa[m:] = 0
+    qb, sfb = _rand_operand(rng, n, k, 0x28, 0x50)
+    gate, res = _gated_inputs(rng, m, n, len(off) - 1)
+    got = oracle.bf16_to_f64(run_gated(h3, qa, sfa, 0.0123, qb, sfb, 2.0 ** -10, m, gate, off, res, gcfg,
+                                       in_place=in_place))
+    R, S = oracle.gemm_reference(qa, sfa, 0.0123, qb, sfb, 2.0 ** -10, k, rows=np.arange(m))
+    lo, hi = oracle.gated_residual_bounds(R, S, gate, off, res)
+    bad = np.argwhere((got < lo) | (got > hi))
+    assert bad.size == 0, f"{len(bad)} outputs outside the bounds, first {bad[:4].tolist()}"

@@ -387,6 +387,23 @@ def test_plain_producer_is_identity_modulation_except_negative_zero():
     assert np.array_equal(np.delete(q_p.ravel(), 5 * 256 + 8), np.delete(q_m.ravel(), 5 * 256 + 8))
 
 
+def test_gated_residual_matches_torch_bf16_ops():
+    """out = RN(res + RN(gate_s * c)): torch's CPU bf16 tensors round every
+    elementwise operation, so `res + gate * c` in bf16 is the same sequence."""
+    g = torch.Generator().manual_seed(43)
+    c = (torch.randn(7, 256, generator=g) * 50).to(torch.bfloat16)
+    gate = torch.randn(3, 256, generator=g).to(torch.bfloat16)
+    res = (torch.randn(7, 256, generator=g) * 20).to(torch.bfloat16)
+    c[0, :4] = torch.tensor([0.0, -0.0, 1e-38, -3e38])
+    gate[0, :4] = torch.tensor([-0.0, 2.0, 1e-3, 0.5])
+    res[0, :4] = torch.tensor([-0.0, -0.0, 1e38, 3e38])
+    off = [0, 2, 2, 7]                      # an empty middle segment
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    out = oracle.gated_residual(bits(c), bits(gate), off, bits(res))
+    gsel = torch.cat([gate[0:1].expand(2, 256), gate[2:3].expand(5, 256)])
+    assert np.array_equal(out, bits(res + gsel * c))
+
+
 # ---------------------------------------------------------------------------
 # GEMM reference
 # ---------------------------------------------------------------------------
