@@ -26,6 +26,7 @@ _STATUS = ctypes.c_int
 _SIGNATURES = {
     "h3fp4_modulate_absmax": ([_P, _I64, _I64, _I64, _P, _P, _I64, _P, _I32, _P, _P, _P], _STATUS),
     "h3fp4_modulate_pack": ([_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _I32, _P, _P, _P, _P], _STATUS),
+    "h3fp4_modulate_produce": ([_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _I32, _P, _P, _P, _P, _P], _STATUS),
     "h3fp4_swiglu_pack": ([_P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P], _STATUS),
     "h3fp4_quantize_pack": ([_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P], _STATUS),
     "h3fp4_gemm_gated_residual": ([_P, _P, _P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I64, _P, _I64, _I64, _I64, _I64,
@@ -101,6 +102,13 @@ def h3fp4_modulate_pack(x, ldx, m, m_pad, d, shift, scale, ld_mod, seg_row_offse
     offs, nseg = _offsets(seg_row_offsets)
     _call("h3fp4_modulate_pack", x, ldx, m, m_pad, d, shift, scale, ld_mod, offs, nseg, tensor_scale, qdata, sfa,
           stream)
+
+
+def h3fp4_modulate_produce(x, ldx, m, m_pad, d, shift, scale, ld_mod, seg_row_offsets, tensor_scale, scratch, qdata,
+                           sfa, stream=0):
+    offs, nseg = _offsets(seg_row_offsets)
+    _call("h3fp4_modulate_produce", x, ldx, m, m_pad, d, shift, scale, ld_mod, offs, nseg, tensor_scale, scratch,
+          qdata, sfa, stream)
 
 
 def h3fp4_swiglu_pack(gate, ldg, up, ldu, m, m_pad, f, tensor_scale, scratch, qdata, sfa, h_workspace=None,
@@ -196,6 +204,27 @@ def modulate_pack(x, shift, scale, seg_row_offsets, tensor_scale, m_pad, *, qdat
     h3fp4_modulate_pack(x.data_ptr(), x.stride(0), m, m_pad, d, shift.data_ptr(), scale.data_ptr(), shift.stride(0),
                         seg_row_offsets, tensor_scale.data_ptr(), qdata.data_ptr(), sfa.data_ptr(), _stream(stream))
     return qdata, sfa
+
+
+def modulate_produce(x, shift, scale, seg_row_offsets, m_pad, *, tensor_scale=None, scratch=None, qdata=None,
+                     sfa=None, stream=None):
+    """Both modulation-producer passes in one launch: returns (tensor_scale, qdata, sfa)."""
+    import torch
+    _need_cuda(x, shift, scale)
+    m, d = x.shape
+    dev = x.device
+    if tensor_scale is None:
+        tensor_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    if scratch is None:
+        scratch = torch.empty(2, dtype=torch.int32, device=dev)
+    if qdata is None:
+        qdata = torch.empty(m_pad, d // 2, dtype=torch.uint8, device=dev)
+    if sfa is None:
+        sfa = torch.empty(sf_bytes(m_pad, d), dtype=torch.uint8, device=dev)
+    h3fp4_modulate_produce(x.data_ptr(), x.stride(0), m, m_pad, d, shift.data_ptr(), scale.data_ptr(),
+                           shift.stride(0), seg_row_offsets, tensor_scale.data_ptr(), scratch.data_ptr(),
+                           qdata.data_ptr(), sfa.data_ptr(), _stream(stream))
+    return tensor_scale, qdata, sfa
 
 
 def swiglu_pack(gate, up, m_pad, *, h_workspace=None, tensor_scale=None, scratch=None, qdata=None, sfa=None,

@@ -112,6 +112,26 @@ h3fp4_status h3fp4_modulate_pack(const void *x_bf16, int64_t ldx, int64_t m, int
         static_cast<const uint16_t *>(scale_bf16), ld_mod, seg, tensor_scale, qdata, sfa, as_stream(stream)));
 }
 
+h3fp4_status h3fp4_modulate_produce(const void *x_bf16, int64_t ldx, int64_t m, int64_t m_pad, int64_t d,
+                                    const void *shift_bf16, const void *scale_bf16, int64_t ld_mod,
+                                    const int32_t *seg_row_offsets, int32_t nseg, float *tensor_scale,
+                                    uint32_t *scratch, uint8_t *qdata, uint8_t *sfa, void *stream)
+{
+    h3fp4_status s = check_modulate(x_bf16, ldx, m, d, shift_bf16, scale_bf16, ld_mod);
+    if (s != H3FP4_OK)
+        return s;
+    if (tensor_scale == nullptr || scratch == nullptr)
+        return H3FP4_ERR_NULL;
+    if ((s = check_pack_outputs(m, m_pad, qdata, sfa)) != H3FP4_OK)
+        return s;
+    SegTable seg;
+    if ((s = make_segments(seg_row_offsets, nseg, m, &seg)) != H3FP4_OK)
+        return s;
+    return from_cuda(h3fp4::launch_modulate_produce(
+        static_cast<const uint16_t *>(x_bf16), ldx, m, m_pad, d, static_cast<const uint16_t *>(shift_bf16),
+        static_cast<const uint16_t *>(scale_bf16), ld_mod, seg, tensor_scale, scratch, qdata, sfa, as_stream(stream)));
+}
+
 h3fp4_status h3fp4_swiglu_pack(const void *gate_bf16, int64_t ldg, const void *up_bf16, int64_t ldu, int64_t m,
                                int64_t m_pad, int64_t f, float *tensor_scale, uint32_t *scratch, uint8_t *qdata,
                                uint8_t *sfa, void *h_workspace, void *stream)

@@ -1039,7 +1039,10 @@ h3fp4_status read_device_error(uint32_t *code)
     const uint32_t zero = 0;
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess)
         return H3FP4_ERR_CUDA;
-    *code = v;
+    uint32_t p = 0;
+    if (read_producer_error(&p) != cudaSuccess)
+        return H3FP4_ERR_CUDA;
+    *code = v | p;
     return H3FP4_OK;
 }
 

@@ -30,6 +30,12 @@ cudaError_t launch_swiglu_pack(const uint16_t *gate, int64_t ldg, const uint16_t
                                int64_t m, int64_t m_pad, int64_t f, float *ts, uint32_t *scratch,
                                uint8_t *qdata, uint8_t *sf, uint16_t *h, cudaStream_t st);
 
+cudaError_t launch_modulate_produce(const uint16_t *x, int64_t ldx, int64_t m, int64_t m_pad, int64_t d,
+                                    const uint16_t *shift, const uint16_t *scale, int64_t ld_mod, const SegTable &seg,
+                                    float *ts, uint32_t *scratch, uint8_t *qdata, uint8_t *sf, cudaStream_t st);
+
+cudaError_t read_producer_error(uint32_t *code);
+
 cudaError_t launch_quantize_pack(const uint16_t *x, int64_t ldx, int64_t m, int64_t m_pad, int64_t d,
                                  float *ts, uint32_t *scratch, uint8_t *qdata, uint8_t *sf, cudaStream_t st);
 

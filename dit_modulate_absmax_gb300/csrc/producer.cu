@@ -28,6 +28,9 @@
 #include "ptx.cuh"
 
 namespace h3fp4 {
+
+// Device error bits of the producer kernels (read and cleared with the GEMM's by read_device_error).
+__device__ uint32_t g_producer_error;
 namespace {
 
 // kSiluLut: uint16[65536], the correctly rounded bf16 silu of every bf16
@@ -291,9 +294,10 @@ __device__ __forceinline__ uint32_t absmax16(const uint32_t (&y)[8])
 // maximum into scratch[0] with one atomicMax, and the last CTA to finish
 // (counted in scratch[1]) converts the maximum into the tensor scale.
 // ---------------------------------------------------------------------------
+// Pass 1 over the tiles blockIdx.x, blockIdx.x + gridDim.x, ...: this thread's
+// maximum |y| bit pattern (the values are also kept by Src, e.g. h).
 template <class Src>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) absmax_kernel(Src src, int64_t m, int col_tiles, int64_t n_tiles,
-                                                          uint32_t *scratch, float *ts_out)
+__device__ __forceinline__ uint32_t absmax_tiles(const Src &src, int64_t m, int col_tiles, int64_t n_tiles)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane & 15, half = lane >> 4;
@@ -324,24 +328,45 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) absmax_kernel(Src src, i
             }
         }
     }
+    return vmax;
+}
+
+// The CTA's maximum of the threads' values (valid in thread 0).
+__device__ __forceinline__ uint32_t cta_max(uint32_t vmax)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     vmax = __reduce_max_sync(0xFFFFFFFFu, vmax);
     __shared__ uint32_t wmax[kWarps];
     if (lane == 0)
         wmax[warp] = vmax;
     __syncthreads();
+    uint32_t mx = 0;
     if (threadIdx.x == 0) {
-        uint32_t mx = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
             mx = max(mx, wmax[w]);
+    }
+    return mx;
+}
+
+// ts = RN_f32(amax / (6 * 448)); a NaN maximum (pattern above 0x7F80) stays NaN.
+__device__ __forceinline__ float tensor_scale_of(uint32_t amax_bits)
+{
+    return __fdiv_rn(__uint_as_float(amax_bits << 16), 2688.0f);
+}
+
+template <class Src>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) absmax_kernel(Src src, int64_t m, int col_tiles, int64_t n_tiles,
+                                                          uint32_t *scratch, float *ts_out)
+{
+    const uint32_t mx = cta_max(absmax_tiles(src, m, col_tiles, n_tiles));
+    if (threadIdx.x == 0) {
         atomicMax(&scratch[0], mx);
         __threadfence();
         const uint32_t done = atomicAdd(&scratch[1], 1u);
         if (done == gridDim.x - 1) {
             __threadfence();
-            const uint32_t a = atomicOr(&scratch[0], 0u);
-            // ts = RN_f32(amax / (6 * 448)); a NaN maximum (pattern above 0x7F80) stays NaN.
-            *ts_out = __fdiv_rn(__uint_as_float(a << 16), 2688.0f);
+            *ts_out = tensor_scale_of(atomicOr(&scratch[0], 0u));
         }
     }
 }
@@ -448,24 +473,20 @@ __device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
 // ---------------------------------------------------------------------------
 // Pass 2: one CTA per 128 x 256 tile (tiles visited in reverse order).
 // ---------------------------------------------------------------------------
+// Pass 2 of output tile t (128 rows x 256 columns): QDATA and the tile's four
+// scale atoms, assembled in the CTA's 2 KB `sft` and written with 16-byte stores.
 template <class Src>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) pack_kernel(Src src, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
-                                                        int64_t n_tiles, const float *ts_ptr, uint8_t *qdata,
-                                                        uint8_t *sf)
+__device__ __forceinline__ void pack_tile(const Src &src, int64_t t, int64_t m, int64_t m_pad, int64_t d,
+                                          int col_tiles, float ts, float den, float rden, bool den_normal,
+                                          uint8_t *qdata, uint8_t *sf, uint8_t *sft)
 {
-    __shared__ __align__(16) uint8_t sft[4 * 512];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane & 15, half = lane >> 4;
-    const int64_t t = n_tiles - 1 - blockIdx.x;
     const int64_t row_tile = t / col_tiles;
     const int col_tile = static_cast<int>(t % col_tiles);
     const int64_t row0 = row_tile * kTileRows;
     const int col = col_tile * kTileCols + sub * kBlock;
     const int64_t qld = d / 2;
-    const float ts = *ts_ptr;
-    const float den = __fmul_rn(6.0f, ts);
-    const bool den_normal = den >= 0x1p-125f && den <= 0x1p125f;
-    const float rden = den_normal ? __frcp_rn(den) : 0.0f;
     typename Src::State st;
     src.begin(st);
 
@@ -502,6 +523,110 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) pack_kernel(Src src, int
     }
 }
 
+struct PackConsts {
+    float ts, den, rden;
+    bool den_normal;
+};
+
+__device__ __forceinline__ PackConsts pack_consts(float ts)
+{
+    PackConsts c;
+    c.ts = ts;
+    c.den = __fmul_rn(6.0f, ts);
+    c.den_normal = c.den >= 0x1p-125f && c.den <= 0x1p125f;
+    c.rden = c.den_normal ? __frcp_rn(c.den) : 0.0f;
+    return c;
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: one CTA per 128 x 256 tile (tiles visited in reverse order).
+// ---------------------------------------------------------------------------
+template <class Src>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) pack_kernel(Src src, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
+                                                        int64_t n_tiles, const float *ts_ptr, uint8_t *qdata,
+                                                        uint8_t *sf)
+{
+    __shared__ __align__(16) uint8_t sft[4 * 512];
+    const PackConsts c = pack_consts(*ts_ptr);
+    pack_tile(src, n_tiles - 1 - blockIdx.x, m, m_pad, d, col_tiles, c.ts, c.den, c.rden, c.den_normal, qdata, sf,
+              sft);
+}
+
+// ---------------------------------------------------------------------------
+// Both passes in one cooperative launch ("NVFP4 Streaming Design", P2 "next":
+// a single-launch cooperative producer, pass 1 and pass 2 around a grid
+// barrier with a bounded wait).  Every CTA of the (co-resident) grid reduces
+// its pass-1 tiles, adds its maximum to scratch[0] and arrives on scratch[1];
+// it then waits until all gridDim.x CTAs have arrived (giving up after 2 s
+// with a device error instead of hanging), derives ts from the global maximum
+// itself and claims pass-2 tiles from a shared counter in reverse order, so
+// that the first tiles packed are the ones pass 1 read last, still in L2, and
+// no CTA waits at the end on a fixed share of slow (fallback-heavy) tiles.
+// ---------------------------------------------------------------------------
+constexpr uint64_t kGridWaitLimitNs = 2000000000ull;
+constexpr uint32_t ERR_GRID_WAIT = 1u << 8;   // the cooperative producer's grid barrier timed out
+
+template <class Src1, class Src2>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+    producer_coop_kernel(Src1 src1, Src2 src2, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
+                         int64_t n_tiles1, int64_t n_tiles2, uint32_t *scratch, float *ts_out, uint8_t *qdata,
+                         uint8_t *sf)
+{
+    __shared__ __align__(16) uint8_t sft[4 * 512];
+    __shared__ float ts_sh;
+    __shared__ int ok_sh;
+    __shared__ uint32_t claim_sh[2];
+    const uint32_t mx = cta_max(absmax_tiles(src1, m, col_tiles, n_tiles1));
+    if (threadIdx.x == 0) {
+        atomicMax(&scratch[0], mx);
+        __threadfence();
+        atomicAdd(&scratch[1], 1u);
+        // grid barrier: every CTA's maximum is in scratch[0] once all have arrived
+        bool ok = true;
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+            uint32_t arrived;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(arrived) : "l"(scratch + 1) : "memory");
+            if (arrived >= gridDim.x)
+                break;
+            if (globaltimer_ns() - t0 > kGridWaitLimitNs) {
+                ok = false;
+                atomicOr(&g_producer_error, ERR_GRID_WAIT);
+                break;
+            }
+            __nanosleep(256);
+        }
+        const float ts = tensor_scale_of(atomicOr(&scratch[0], 0u));
+        if (ok && blockIdx.x == 0)
+            *ts_out = ts;
+        ts_sh = ts;
+        ok_sh = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!ok_sh)
+        return;
+    // Pass 2 hands tiles out dynamically: past the barrier scratch[1] only
+    // grows from gridDim.x, so each atomicAdd on it claims the next tile
+    // (claim - gridDim.x, counted from the end).  Thread 0 claims one tile
+    // ahead into the other slot of claim_sh while the CTA packs the current one.
+    const PackConsts c = pack_consts(ts_sh);
+    int slot = 0;
+    if (threadIdx.x == 0)
+        claim_sh[0] = atomicAdd(&scratch[1], 1u) - gridDim.x;
+    __syncthreads();
+    while (true) {
+        const uint32_t idx = claim_sh[slot];
+        if (idx >= n_tiles2)
+            break;
+        if (threadIdx.x == 0)
+            claim_sh[slot ^ 1] = atomicAdd(&scratch[1], 1u) - gridDim.x;
+        pack_tile(src2, n_tiles2 - 1 - static_cast<int64_t>(idx), m, m_pad, d, col_tiles, c.ts, c.den, c.rden,
+                  c.den_normal, qdata, sf, sft);
+        __syncthreads();   // sft and the claim slot just read are reused by the next tile
+        slot ^= 1;
+    }
+}
+
 // Logical [rows, cols] (leading dimension ld) -> 128x4-atom scale layout.
 __global__ void swizzle_kernel(const uint8_t *src, int64_t rows, int64_t cols, int64_t ld, uint8_t *dst,
                                int64_t total)
@@ -530,6 +655,39 @@ cudaError_t run_absmax(const Src &src, int64_t m, int64_t d, float *ts, uint32_t
     const int grid = static_cast<int>(n_tiles < cap ? n_tiles : cap);
     absmax_kernel<Src><<<grid, kThreads, 0, st>>>(src, m, col_tiles, n_tiles, scratch, ts);
     return cudaGetLastError();
+}
+
+// Both passes in one cooperative launch: a grid of co-resident CTAs (the
+// occupancy-derived count, capped by the tile count) so that the in-kernel
+// grid barrier cannot wait on a CTA that is not running.
+template <class Src1, class Src2>
+cudaError_t run_coop(const Src1 &src1, const Src2 &src2, int64_t m, int64_t m_pad, int64_t d, float *ts,
+                     uint32_t *scratch, uint8_t *qdata, uint8_t *sf, cudaStream_t st)
+{
+    const int col_tiles = static_cast<int>(d / kTileCols);
+    const int64_t n_tiles1 = ((m + kTileRows - 1) / kTileRows) * col_tiles;
+    const int64_t n_tiles2 = ((m_pad + kTileRows - 1) / kTileRows) * col_tiles;
+    if (n_tiles2 == 0)
+        return m == 0 ? cudaMemsetAsync(ts, 0, sizeof(float), st) : cudaSuccess;
+    cudaError_t e = cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), st);
+    if (e != cudaSuccess)
+        return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, producer_coop_kernel<Src1, Src2>, kThreads, 0);
+    if (e != cudaSuccess)
+        return e;
+    if (per_sm < 1)
+        return cudaErrorCooperativeLaunchTooLarge;
+    const int64_t resident = static_cast<int64_t>(per_sm) * sm_count();
+    const int64_t want = n_tiles2 > n_tiles1 ? n_tiles2 : n_tiles1;
+    const unsigned grid = static_cast<unsigned>(want < resident ? want : resident);
+    if (n_tiles2 + 2ll * grid >= 0xFFFFFFFFll)   // the 32-bit arrival/claim counter must not wrap
+        return cudaErrorInvalidValue;
+    void *args[] = {const_cast<Src1 *>(&src1), const_cast<Src2 *>(&src2), &m, &m_pad, &d,
+                    const_cast<int *>(&col_tiles), const_cast<int64_t *>(&n_tiles1), const_cast<int64_t *>(&n_tiles2),
+                    &scratch, &ts, &qdata, &sf};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(producer_coop_kernel<Src1, Src2>), dim3(grid),
+                                       dim3(kThreads), args, 0, st);
 }
 
 template <class Src>
@@ -585,10 +743,27 @@ cudaError_t launch_quantize_pack(const uint16_t *x, int64_t ldx, int64_t m, int6
                                  uint32_t *scratch, uint8_t *qdata, uint8_t *sf, cudaStream_t st)
 {
     PlainSrc src{x, ldx};
-    cudaError_t e = run_absmax(src, m, d, ts, scratch, st);
+    return run_coop(src, src, m, m_pad, d, ts, scratch, qdata, sf, st);
+}
+
+cudaError_t launch_modulate_produce(const uint16_t *x, int64_t ldx, int64_t m, int64_t m_pad, int64_t d,
+                                    const uint16_t *shift, const uint16_t *scale, int64_t ld_mod, const SegTable &seg,
+                                    float *ts, uint32_t *scratch, uint8_t *qdata, uint8_t *sf, cudaStream_t st)
+{
+    ModulateSrc src{x, ldx, shift, scale, ld_mod, seg};
+    return run_coop(src, src, m, m_pad, d, ts, scratch, qdata, sf, st);
+}
+
+cudaError_t read_producer_error(uint32_t *code)
+{
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_producer_error, sizeof(v));
     if (e != cudaSuccess)
         return e;
-    return run_pack(src, m, m_pad, d, ts, qdata, sf, st);
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_producer_error, &zero, sizeof(zero));
+    *code = v;
+    return e;
 }
 
 cudaError_t launch_swiglu_pack(const uint16_t *gate, int64_t ldg, const uint16_t *up, int64_t ldu, int64_t m,
@@ -596,15 +771,12 @@ cudaError_t launch_swiglu_pack(const uint16_t *gate, int64_t ldg, const uint16_t
                                uint16_t *h, cudaStream_t st)
 {
     SwigluSrc src{gate, ldg, up, ldu, h, f};
-    cudaError_t e = run_absmax(src, m, f, ts, scratch, st);
-    if (e != cudaSuccess)
-        return e;
-    if (h != nullptr && m > 0) {
+    if (h != nullptr) {   // pass 1 keeps h, pass 2 packs it after the grid barrier
         PlainSrc plain{h, f};
-        return run_pack(plain, m, m_pad, f, ts, qdata, sf, st);
+        return run_coop(src, plain, m, m_pad, f, ts, scratch, qdata, sf, st);
     }
     SwigluSrc recompute{gate, ldg, up, ldu, nullptr, f};
-    return run_pack(recompute, m, m_pad, f, ts, qdata, sf, st);
+    return run_coop(src, recompute, m, m_pad, f, ts, scratch, qdata, sf, st);
 }
 
 cudaError_t launch_swizzle_scales(const uint8_t *src, int64_t rows, int64_t cols, int64_t ld, uint8_t *dst,

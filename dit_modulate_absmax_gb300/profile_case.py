@@ -1,11 +1,12 @@
 """Runs one hot-path call on synthetic inputs, for profilers.
 
-  python -m dit_modulate_absmax_gb300.profile_case {modulate,swiglu,gemm} [--m M] [--n N] [--k K] [--reps R]
-      [--workspace] [--cta-pair P] [--n-group G]
+  python -m dit_modulate_absmax_gb300.profile_case {modulate,swiglu,plain,gemm} [--m M] [--n N] [--k K] [--reps R]
+      [--workspace] [--single-launch] [--cta-pair P] [--n-group G]
 
 `modulate` runs both passes of the modulation producer on an [M, K]
 activation, `swiglu` the SwiGLU producer on [M, K] gate/up (with
-`--workspace`, the form the benchmark times: pass 1 keeps h), `gemm` the
+`--workspace`, the form the benchmark times: pass 1 keeps h), `plain` the
+plain-activation producer on an [M, K] bf16 activation, `gemm` the
 block-scaled GEMM of a packed [M, K] activation with a packed [N, K] weight.
 The R timed repetitions run between cudaProfilerStart and cudaProfilerStop
 (so `ncu --profile-from-start off` sees only them) after two warm-up calls,
@@ -25,20 +26,22 @@ from dit_modulate_absmax_gb300 import workloads as W
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=("modulate", "swiglu", "gemm"))
+    ap.add_argument("op", choices=("modulate", "swiglu", "plain", "gemm"))
     ap.add_argument("--m", type=int, default=W.M_TOKENS)
     ap.add_argument("--n", type=int, default=21504)
     ap.add_argument("--k", type=int, default=7168)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--cta-pair", type=int, default=0, help="GEMM kernel: 0 default, 1 single CTA, 2 CTA pairs")
     ap.add_argument("--n-group", type=int, default=0, help="GEMM N-group (0 = default)")
+    ap.add_argument("--single-launch", action="store_true",
+                    help="modulate: both passes in one cooperative launch (h3fp4_modulate_produce)")
     ap.add_argument("--workspace", action="store_true",
                     help="swiglu: keep h in a workspace (pass 1 writes it, pass 2 packs from it)")
     a = ap.parse_args()
     B.build()
     dev = torch.device("cuda")
     m_pad = -(-a.m // 16) * 16
-    base = W.WORKLOADS["fc2" if a.op == "swiglu" else "qkv"]
+    base = W.WORKLOADS[{"swiglu": "fc2", "plain": "h3_attn"}.get(a.op, "qkv")]
     w = dataclasses.replace(base, m=a.m, m_pad=m_pad, k=a.k, n=a.n,
                             seg_off=(0, min(32768, a.m), a.m) if base.kind == "modulate" else ())
     act = W.activations(w, device=dev)
@@ -53,8 +56,15 @@ def main():
         def call():
             h3.swiglu_pack(act["gate"], act["up"], m_pad, h_workspace=hw, tensor_scale=ts, scratch=scratch, qdata=q,
                            sfa=sfa)
+    elif a.op == "plain":
+        def call():
+            h3.quantize_pack(act["x"], m_pad, tensor_scale=ts, scratch=scratch, qdata=q, sfa=sfa)
     else:
         def produce():
+            if a.single_launch:
+                h3.modulate_produce(act["x"], act["shift"], act["scale"], off, m_pad, tensor_scale=ts,
+                                    scratch=scratch, qdata=q, sfa=sfa)
+                return
             h3.modulate_absmax(act["x"], act["shift"], act["scale"], off, tensor_scale=ts, scratch=scratch)
             h3.modulate_pack(act["x"], act["shift"], act["scale"], off, ts, m_pad, qdata=q, sfa=sfa)
         call = produce

@@ -116,7 +116,25 @@ H3FP4_API h3fp4_status h3fp4_modulate_pack(const void *x_bf16, int64_t ldx, int6
                                  void *stream);
 
 /*
- * h3fp4_swiglu_pack -- SwiGLU-fused producer (both passes).
+ * h3fp4_modulate_produce -- h3fp4_modulate_absmax followed by
+ * h3fp4_modulate_pack in ONE cooperative launch.
+ * Source: "NVFP4 Streaming Design", P2 (a single-launch cooperative producer:
+ * pass 1 and pass 2 around a grid barrier, with a bounded wait).
+ *
+ * Same arguments and results as the two calls (tensor_scale is written and
+ * also used by the pack).  Every CTA of the co-resident grid reduces its
+ * pass-1 tiles, arrives on a grid barrier in `scratch` and packs its pass-2
+ * tiles once all have arrived; the barrier gives up after 2 s, reporting
+ * bit 8 through h3fp4_device_error instead of hanging.
+ */
+H3FP4_API h3fp4_status h3fp4_modulate_produce(const void *x_bf16, int64_t ldx, int64_t m, int64_t m_pad,
+                                    int64_t d, const void *shift_bf16, const void *scale_bf16,
+                                    int64_t ld_mod, const int32_t *seg_row_offsets, int32_t nseg,
+                                    float *tensor_scale, uint32_t *scratch, uint8_t *qdata,
+                                    uint8_t *sfa, void *stream);
+
+/*
+ * h3fp4_swiglu_pack -- SwiGLU-fused producer (both passes, in one cooperative launch).
  * Source: "FC2 NVFP4 Library Scheduling", Exact Operation and Current Baseline
  * (exact BF16 SwiGLU fused into NVFP4 production of the FC2 input).
  *
@@ -139,7 +157,7 @@ H3FP4_API h3fp4_status h3fp4_swiglu_pack(const void *gate_bf16, int64_t ldg, con
 
 /*
  * h3fp4_quantize_pack -- NVFP4 producer of an activation that needs no fused
- * transform (both passes).
+ * transform (both passes, in one cooperative launch).
  * Source: "NVFP4 Modulation Producer Fusion", Change Summary (the same two-pass
  * producer: global absmax -> FP32 tensor scale, then E4M3 block scales and
  * E2M1 codes); "NVFP4 Streaming Design", P0 and P2 (the attention-output

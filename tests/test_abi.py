@@ -97,6 +97,16 @@ def test_swiglu_pack_validation(L):
     assert f(F, 256, F, 256, 10, 4, 256, F, F, F, F, None, None) == SHAPE
 
 
+def test_modulate_produce_validation(L):
+    f = L.h3fp4_modulate_produce
+    offs = (ctypes.c_int32 * 2)(0, 10)
+    assert f(None, 256, 10, 16, 256, F, F, 256, offs, 1, F, F, F, F, None) == NULL
+    assert f(F, 256, 10, 16, 256, F, F, 256, offs, 1, None, F, F, F, None) == NULL     # tensor scale
+    assert f(F, 256, 10, 16, 300, F, F, 256, offs, 1, F, F, F, F, None) == SHAPE
+    assert f(F, 256, 10, 4, 256, F, F, 256, offs, 1, F, F, F, F, None) == SHAPE       # m_pad < m
+    assert f(F, 256, 10, 16, 256, F, F, 256, (ctypes.c_int32 * 2)(0, 9), 1, F, F, F, F, None) == SHAPE
+
+
 def test_quantize_pack_validation(L):
     f = L.h3fp4_quantize_pack
     assert f(None, 256, 10, 16, 256, F, F, F, F, None) == NULL

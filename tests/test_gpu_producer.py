@@ -282,6 +282,29 @@ def test_plain_zero_rows(h3):
     assert ts == 0.0 and not q.any() and not sfa.any()
 
 
+@pytest.mark.parametrize("m,m_pad,d,off", [
+    (0, 16, 256, [0, 0]),
+    (1, 16, 256, [0, 1]),
+    (300, 320, 768, [0, 0, 150, 300]),
+    (16384 + 77, 16512, 4096, [0, 8000, 16461]),      # more tiles than the co-resident grid
+])
+def test_single_launch_modulation_producer(h3, m, m_pad, d, off):
+    """Both passes in one cooperative launch: the same bytes as the oracle (and
+    so as the two-call path), every tile packed after the grid barrier."""
+    x, sh, sc = _random_case(m, d, len(off) - 1, seed=m + 3 * d)
+    ts_o, q_o, sf_o, _, _ = oracle.modulate_producer(x, sh, sc, off, m_pad)
+    xd = _to_dev(x) if m else torch.empty(0, d, dtype=torch.int16, device="cuda")
+    q = torch.full((m_pad, d // 2), CANARY, dtype=torch.uint8, device="cuda")
+    sfa = torch.full((h3.sf_bytes(m_pad, d),), CANARY, dtype=torch.uint8, device="cuda")
+    ts = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    h3.modulate_produce(xd, _to_dev(sh), _to_dev(sc), off, m_pad, tensor_scale=ts, qdata=q, sfa=sfa)
+    torch.cuda.synchronize()
+    assert h3.h3fp4_device_error() == 0
+    assert _f32_bits(float(ts.item())) == _f32_bits(ts_o)
+    assert np.array_equal(q.cpu().numpy(), q_o)
+    assert np.array_equal(sfa.cpu().numpy(), oracle.swizzle_sf(sf_o))
+
+
 def test_swizzle_kernel_matches_oracle_layout(h3):
     rng = np.random.default_rng(17)
     for rows, cols in [(384, 16), (300, 64), (1, 4), (129, 896)]:
