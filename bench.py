@@ -444,9 +444,10 @@ def main():
                     help="linear set: the benchmark's configs (default) or the model's own projection widths")
     ap.add_argument("--gated", action="store_true",
                     help="--widths h3: attention output and FC2 use the gated residual epilogue")
-    ap.add_argument("--gemm-kernel", type=int, default=0, choices=(0, 1, 2, 3),
-                    help="GEMM kernel (h3fp4_gemm_config.cta_pair): 0 library default, 1 single CTA, "
-                         "2 CTA pair, 3 two-CTA cluster with B multicast")
+    ap.add_argument("--gemm-kernel", type=int, default=0, choices=(0, 1, 2, 3, 4),
+                    help="GEMM kernel (h3fp4_gemm_config.cta_pair): 0 library default (4), 1 single CTA, "
+                         "2 CTA pair with scale warps, 3 two-CTA cluster with B multicast, "
+                         "4 CTA pair with the scales copied into TMEM by the MMA warp")
     ap.add_argument("--profile-range", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()

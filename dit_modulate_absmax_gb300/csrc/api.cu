@@ -186,7 +186,7 @@ h3fp4_status check_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_
     *c = h3fp4_gemm_config{0, 0, 0, 0};
     if (cfg != nullptr) {
         *c = *cfg;
-        if (c->n_group < 0 || c->stages != 0 || c->cta_pair < 0 || c->cta_pair > 3 || c->reserved != 0)
+        if (c->n_group < 0 || c->stages != 0 || c->cta_pair < 0 || c->cta_pair > 4 || c->reserved != 0)
             return H3FP4_ERR_UNSUPPORTED;
     }
     return H3FP4_OK;

@@ -72,6 +72,7 @@ constexpr int kScaleWarps = 4;                     // one per TMEM lane quarter
 constexpr int kFirstEpiWarp = 2;
 constexpr int kFirstScaleWarp = kFirstEpiWarp + kEpiWarps;
 constexpr int kThreads = 32 * (2 + kEpiWarps + kScaleWarps);
+constexpr int kThreadsCp = 32 * (2 + kEpiWarps);   // scales copied by the MMA warp: no scale warps
 constexpr int kDefaultNGroup = 28;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
@@ -824,6 +825,219 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace pair
 
+// ---------------------------------------------------------------------------
+// CTA-pair kernel with the scales copied by the MMA warp (cta_group::2
+// tcgen05.cp).  Per K step each CTA loads, into one stage of a 5-stage ring,
+// its 128 rows of A, its 128 rows of B, its A scale atoms and all 256 rows'
+// B scale atoms, every load completing on the leader's full barrier (the
+// cta_group::2 form of the tensor copy; out-of-range boxes, e.g. the absent
+// second row block of the last M tile, are zero-filled and still count their
+// full size).  The leader's MMA warp, warp-collectively, copies the stage's 12
+// scale atoms into both CTAs' TMEM slot for that stage (each CTA's shared
+// memory into its own TMEM), issues the 4 pair MMAs and commits the stage
+// free in both CTAs.  No scale warps and no per-step hand-off between the
+// SMs other than the loads' own completion.  Each CTA's epilogue drains its
+// own 128 accumulator rows; kGated selects the gated residual epilogue.
+// ---------------------------------------------------------------------------
+namespace paircp {
+
+constexpr int kStages = 5;
+constexpr uint32_t STAGE_TX = 2 * (pair::A_BYTES + pair::B_BYTES + pair::SFA_BYTES + pair::SFB_BYTES);
+
+struct __align__(1024) Smem {
+    uint8_t a[kStages][pair::A_BYTES];
+    uint8_t b[kStages][pair::B_BYTES];
+    uint8_t sfa[kStages][pair::SFA_BYTES];
+    uint8_t sfb[kStages][pair::SFB_BYTES];
+    uint8_t cst[kEpiWarps][CST_BYTES];  // per epilogue warp: output staging for tensor stores
+    uint64_t res_full[kEpiWarps];       // per epilogue warp: a residual block landed in cst (gated epilogue)
+    uint64_t full[kStages];             // leader: both CTAs' operands and scales landed
+    uint64_t empty[kStages];            // both CTAs, arrived by the leader's commits
+    uint64_t acc_full;                  // both CTAs
+    uint64_t acc_empty;                 // used in the leader
+    uint32_t tmem_base;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(SF_COL + kStages * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM scale slots");
+
+template <bool kGated>
+__global__ void __launch_bounds__(kThreadsCp, 1)
+    nvf4_gemm_pair_cp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
+                             const __grid_constant__ GatedEpilogue ge, const float *__restrict__ a_ts,
+                             const float *__restrict__ b_ts, int m, int n, int k, int m_tiles2, int n_tiles,
+                             int n_group)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+    const int kt_count = k / BK;
+    const int chunks_per_rb = k / 256;          // 2 KB scale chunks per 128-row block
+    const int total_tiles = m_tiles2 * n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
+        }
+        mbar_init(smem_u32(&sm.acc_full), 1);
+        mbar_init(smem_u32(&sm.acc_empty), 2 * kEpiWarps);
+        for (int w = 0; w < kEpiWarps; ++w)
+            mbar_init(smem_u32(&sm.res_full[w]), 1);
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmSFA);
+        prefetch_tmap(&tmSFB);
+        prefetch_tmap(&tmC);
+        if (kGated)
+            prefetch_tmap(&tmR);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&sm.tmem_base), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = pair_id; t < total_tiles && ok; t += num_pairs) {
+                int mt2, nt;
+                tile_coords(t, m_tiles2, n_tiles, n_group, mt2, nt);
+                const int rb_a = 2 * mt2 + static_cast<int>(rank);
+                for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ((it / kStages) & 1) ^ 1u, kWaitLimitNs)) {
+                        record_error(ERR_WAIT_EMPTY);
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(smem_u32(&sm.full[s]), STAGE_TX);
+                    const uint32_t bar = mapa_shared(smem_u32(&sm.full[s]), 0);
+                    tma_load_2d_pair(smem_u32(sm.sfa[s]), &tmSFA, 0, (rb_a * chunks_per_rb + kt) * 8, bar);
+                    tma_load_2d_pair(smem_u32(sm.sfb[s]), &tmSFB, 0, (2 * nt * chunks_per_rb + kt) * 8, bar);
+                    tma_load_2d_pair(smem_u32(sm.sfb[s]) + pair::SFB_BYTES / 2, &tmSFB, 0,
+                                     ((2 * nt + 1) * chunks_per_rb + kt) * 8, bar);
+                    tma_load_2d_pair(smem_u32(sm.a[s]), &tmA, kt * BKB, mt2 * 256 + static_cast<int>(rank) * 128, bar);
+                    tma_load_2d_pair(smem_u32(sm.b[s]), &tmB, kt * BKB, nt * pair::BN + static_cast<int>(rank) * 128,
+                                     bar);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (rank == 0) {
+            constexpr uint32_t idesc = idesc_nvf4(2 * pair::BM, pair::BN);
+            uint32_t it = 0, local = 0;
+            bool ok = true;
+            for (int t = pair_id; t < total_tiles && ok; t += num_pairs, ++local) {
+                if (!warp_wait(smem_u32(&sm.acc_empty), (local & 1) ^ 1u)) {
+                    if (lane == 0)
+                        record_error(ERR_WAIT_ACC_EMPTY);
+                    break;
+                }
+                tc_fence_after();
+                for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                    const int s = it % kStages;
+                    if (!warp_wait(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
+                        if (lane == 0)
+                            record_error(ERR_WAIT_FULL);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + SF_COL + s * SF_COLS_PER_STAGE;
+                    const uint32_t sfb_t = sfa_t + 16;
+                    const uint32_t sfa_s = smem_u32(sm.sfa[s]), sfb_s = smem_u32(sm.sfb[s]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        tc_cp_32x128b_warpx4_pair_elect(sfa_t + 4 * j, smem_desc(sfa_s + j * ATOM, 0, 128, 0));
+                        tc_cp_32x128b_warpx4_pair_elect(sfb_t + 8 * j, smem_desc(sfb_s + j * ATOM, 0, 128, 0));
+                        tc_cp_32x128b_warpx4_pair_elect(sfb_t + 8 * j + 4,
+                                                        smem_desc(sfb_s + pair::SFB_BYTES / 2 + j * ATOM, 0, 128, 0));
+                    }
+                    const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, 1024, 2);
+                    const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, 1024, 2);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tc_mma_nvf4_pair_elect(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, idesc, sfa_t + 4 * j,
+                                               sfb_t + 8 * j, (kt | j) != 0);
+                    tc_commit_pair_mc_elect(smem_u32(&sm.empty[s]), 0x3);
+                }
+                if (ok)
+                    tc_commit_pair_mc_elect(smem_u32(&sm.acc_full), 0x3);
+            }
+        }
+    } else {
+        const int q = warp & 3;
+        const int half = (warp - kFirstEpiWarp) >> 2;
+        const float alpha = __fmul_rn(*a_ts, *b_ts);
+        const uint32_t leader_acc_empty = mapa_shared(smem_u32(&sm.acc_empty), 0);
+        uint32_t local = 0, rphase = 0;
+        for (int t = pair_id; t < total_tiles; t += num_pairs, ++local) {
+            int mt2, nt;
+            tile_coords(t, m_tiles2, n_tiles, n_group, mt2, nt);
+            if (!warp_wait(smem_u32(&sm.acc_full), local & 1)) {
+                if (lane == 0)
+                    record_error(ERR_WAIT_ACC);
+                break;
+            }
+            tc_fence_after();
+            uint32_t pk[64];
+            const uint32_t base = tmem + (static_cast<uint32_t>(q * 32) << 16) + ACC_COL + half * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(base + 32 * c, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float lo = __fmul_rn(alpha, __uint_as_float(v[2 * i]));
+                    const float hi = __fmul_rn(alpha, __uint_as_float(v[2 * i + 1]));
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                    memcpy(&pk[16 * c + i], &b2, 4);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)   // this CTA's rows are drained (relaxed: earlier tiles' stores need not land first)
+                mbar_arrive_cluster_relaxed(leader_acc_empty);
+            const int row0 = mt2 * 256 + static_cast<int>(rank) * pair::BM + q * 32;
+            if (kGated) {
+                if (!store_rows_gated(&tmC, &tmR, smem_u32(sm.cst[warp - kFirstEpiWarp]),
+                                      smem_u32(&sm.res_full[warp - kFirstEpiWarp]), rphase, pk,
+                                      nt * pair::BN + half * 128, row0, lane, gate_row(ge, row0 + lane))) {
+                    if (lane == 0)
+                        record_error(ERR_WAIT_ACC);
+                    break;
+                }
+            } else {
+                store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpiWarp]), pk, nt * pair::BN + half * 128, row0, lane);
+            }
+        }
+        if (lane == 0)
+            bulk_wait_group0();
+    }
+
+    tc_fence_before();
+    cluster_sync();   // no CTA leaves while its peer may still touch its barriers or TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace paircp
+
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -996,34 +1210,110 @@ h3fp4_status launch_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
 
 }  // namespace
 
+// Tensor map of the residual and the kernel-parameter copy of the gate
+// arguments (both unused without a gated epilogue).
+bool make_gated(const GatedArgs *gated, const CUtensorMap &tmC, int64_t m, int64_t n, CUtensorMap *tmR,
+                GatedEpilogue *ge)
+{
+    *ge = GatedEpilogue{};
+    if (gated == nullptr) {
+        *tmR = tmC;
+        return true;
+    }
+    if (!make_output_map(tmR, const_cast<void *>(gated->residual), m, n, gated->ldr))
+        return false;
+    ge->gate = gated->gate;
+    ge->ld_gate = gated->ld_gate;
+    for (int i = 0; i <= H3FP4_MAX_SEGMENTS; ++i)
+        ge->off[i] = gated->seg.off[i];
+    ge->nseg = gated->seg.nseg;
+    return true;
+}
+
+template <bool kGated>
+cudaError_t set_pair_cp_smem()
+{
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(paircp::nvf4_gemm_pair_cp_kernel<kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(paircp::kSmemBytes));
+        if (e != cudaSuccess)
+            return e;
+        attr_set[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
+                            const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m,
+                            int64_t m_pad, int64_t n, int64_t k, int n_group_cfg, const GatedArgs *gated,
+                            cudaStream_t st)
+{
+    const int64_t sfa_rows = (m_pad + 127) / 128 * 128, sfb_rows = (n + 127) / 128 * 128;
+    CUtensorMap tmA, tmB, tmSFA, tmSFB, tmC, tmR;
+    GatedEpilogue ge;
+    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, pair::BM) || !make_operand_map(&tmB, b_q, n, k / 2, 128) ||
+        !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16)) || !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16)) ||
+        !make_output_map(&tmC, c, m, n, ldc) || !make_gated(gated, tmC, m, n, &tmR, &ge))
+        return H3FP4_ERR_CUDA;
+    if ((gated ? set_pair_cp_smem<true>() : set_pair_cp_smem<false>()) != cudaSuccess)
+        return H3FP4_ERR_CUDA;
+    const int m_tiles2 = static_cast<int>((m + 255) / 256);
+    const int n_tiles = static_cast<int>((n + pair::BN - 1) / pair::BN);
+    const int64_t total = static_cast<int64_t>(m_tiles2) * n_tiles;
+    if (total > 0x7FFFFFFF)
+        return H3FP4_ERR_SHAPE;
+    int n_group = n_group_cfg > 0 ? n_group_cfg : kDefaultNGroup;
+    if (n_group > n_tiles)
+        n_group = n_tiles;
+    const int max_pairs = sm_count() / 2;
+    const int pairs = static_cast<int>(total < max_pairs ? total : max_pairs);
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(2 * pairs, 1, 1);
+    lc.blockDim = dim3(kThreadsCp, 1, 1);
+    lc.dynamicSmemBytes = paircp::kSmemBytes;
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const cudaError_t e =
+        gated ? cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<true>, tmA, tmB, tmSFA, tmSFB, tmC, tmR, ge,
+                                   a_ts, b_ts, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), m_tiles2,
+                                   n_tiles, n_group)
+              : cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<false>, tmA, tmB, tmSFA, tmSFB, tmC, tmR, ge,
+                                   a_ts, b_ts, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), m_tiles2,
+                                   n_tiles, n_group);
+    return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
+}
+
 h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
                          const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m, int64_t m_pad,
                          int64_t n, int64_t k, const h3fp4_gemm_config &cfg, const GatedArgs *gated, cudaStream_t st)
 {
     if (m == 0 || n == 0)
         return H3FP4_OK;
+    if (cfg.cta_pair == 0 || cfg.cta_pair == 4)   // the default: measured fastest in the DiT step
+        return launch_pair_cp(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, gated, st);
     if (cfg.cta_pair == 2) {
         if (gated != nullptr)
             return H3FP4_ERR_UNSUPPORTED;
         return launch_pair(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, st);
     }
-    const bool mcast = cfg.cta_pair == 3 || cfg.cta_pair == 0;   // the default: measured fastest in the DiT step
+    const bool mcast = cfg.cta_pair == 3;
     CUtensorMap tmA, tmB, tmC, tmR;
+    GatedEpilogue ge;
     if (!make_operand_map(&tmA, a_q, m_pad, k / 2, BM) ||
-        !make_operand_map(&tmB, b_q, n, k / 2, mcast ? BN / 2 : BN) || !make_output_map(&tmC, c, m, n, ldc))
+        !make_operand_map(&tmB, b_q, n, k / 2, mcast ? BN / 2 : BN) || !make_output_map(&tmC, c, m, n, ldc) ||
+        !make_gated(gated, tmC, m, n, &tmR, &ge))
         return H3FP4_ERR_CUDA;
-    GatedEpilogue ge{};
-    if (gated != nullptr) {
-        if (!make_output_map(&tmR, const_cast<void *>(gated->residual), m, n, gated->ldr))
-            return H3FP4_ERR_CUDA;
-        ge.gate = gated->gate;
-        ge.ld_gate = gated->ld_gate;
-        for (int i = 0; i <= H3FP4_MAX_SEGMENTS; ++i)
-            ge.off[i] = gated->seg.off[i];
-        ge.nseg = gated->seg.nseg;
-    } else {
-        tmR = tmC;   // unused
-    }
     if (mcast)
         return gated ? launch_tiles<true, true>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st)
                      : launch_tiles<true, false>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st);

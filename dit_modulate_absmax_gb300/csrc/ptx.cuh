@@ -184,6 +184,53 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// Warp-collective forms of the tcgen05 issue: the whole warp executes the
+// instruction and one lane (elect.sync: the lowest active lane) issues it, so
+// the operands stay warp-uniform.  Issued from a one-lane branch instead, each
+// tcgen05 instruction measured ~30 cycles of extra issue cost, enough to make
+// 12 scale-atom copies per K step cost 370 cycles on top of the 4 MMAs; issued
+// warp-collectively they run under the MMAs for free.  All lanes of the warp
+// must be active; the issuing lane is then lane 0 for every call, so that a
+// later commit from lane 0 (or from tc_commit_elect) covers these operations.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_elect(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(sdesc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_nvf4_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 q, %6, 0;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_mc_elect(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
 // Arrives once on the mbarrier when all previously issued tcgen05 async
 // operations of this thread have completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar)
@@ -374,6 +421,40 @@ __device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t a_des
         "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
         " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Warp-collective (elect.sync) forms of the pair copy, MMA and commit; see
+// tc_cp_32x128b_warpx4_elect.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair_elect(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(sdesc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_nvf4_pair_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                       uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 q, %6, 0;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair_mc_elect(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+        "h"(mask)
         : "memory");
 }
 

@@ -186,12 +186,14 @@ typedef struct h3fp4_gemm_config {
      * clamped). */
     int32_t n_group;
     int32_t stages;    /* reserved, must be 0 (the pipeline depth is fixed per kernel) */
-    /* GEMM kernel: 0 = library default (currently 3), 1 = one CTA per 128 x 256 output tile
-     * (4-stage ring), 2 = CTA pairs on two SMs per 256 x 256 tile (tcgen05
-     * cta_group::2, each SM loads half of A and half of B; 6-stage ring),
-     * 3 = clusters of two CTAs on the two 128 x 256 tiles of one 256 x 256
-     * block, each loading its own A and half of the shared B tile, multicast
-     * into both (4-stage ring). */
+    /* GEMM kernel: 0 = library default (currently 4), 1 = one CTA per 128 x 256 output tile
+     * (4-stage ring, scale warps stage the scales in TMEM), 2 = CTA pairs on
+     * two SMs per 256 x 256 tile (tcgen05 cta_group::2, each SM loads half of
+     * A and half of B; 6-stage ring; scale warps; no gated epilogue), 3 =
+     * clusters of two CTAs on the two 128 x 256 tiles of one 256 x 256 block,
+     * each loading its own A and half of the shared B tile, multicast into
+     * both (4-stage ring, scale warps), 4 = CTA pairs as 2 whose MMA warp
+     * copies the scales into TMEM itself (tcgen05.cp; 5-stage ring). */
     int32_t cta_pair;
     int32_t reserved;  /* must be 0 */
 } h3fp4_gemm_config;

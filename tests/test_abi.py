@@ -134,7 +134,7 @@ def test_gemm_validation(L):
     assert call(cfg=ctypes.byref(bad)) == UNSUP
     bad = pkg.GemmConfig(0, 3, 0, 0)
     assert call(cfg=ctypes.byref(bad)) == UNSUP
-    bad = pkg.GemmConfig(0, 0, 4, 0)       # kernels are 0 (default) .. 3
+    bad = pkg.GemmConfig(0, 0, 5, 0)       # kernels are 0 (default) .. 4
     assert call(cfg=ctypes.byref(bad)) == UNSUP
 
 
@@ -153,7 +153,7 @@ def test_gemm_gated_residual_validation(L):
     assert call(ldr=388) == ALIGN
     assert call(off=(ctypes.c_int32 * 3)(0, 250, 200)) == SHAPE          # offsets must not decrease
     assert call(residual=F + 64) == UNSUP                                 # partial overlap with the output
-    assert call(cfg=ctypes.byref(pkg.GemmConfig(0, 0, 2, 0))) == UNSUP     # the pair kernel has no gated form
+    assert call(cfg=ctypes.byref(pkg.GemmConfig(0, 0, 2, 0))) == UNSUP     # the scale-warp pair kernel has no gated form
 
 
 def test_swizzle_and_device_error_validation(L):
