@@ -129,6 +129,11 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # profile summary -> traffic of the dominant kernel (only while its source is unchanged)
 # ----------------------------------------------------------------------------
+# kernel behind each h3fp4_gemm_config.cta_pair value (0 = the library default)
+GEMM_KERNELS = {0: "nvf4_gemm_pair_cp_kernel", 1: "nvf4_gemm_kernel<single CTA>", 2: "nvf4_gemm_pair_kernel",
+                3: "nvf4_gemm_kernel<multicast pair>", 4: "nvf4_gemm_pair_cp_kernel"}
+
+
 def _gemm_source_sha():
     h = hashlib.sha256()
     for f in ("gemm.cu", "ptx.cuh"):
@@ -348,9 +353,10 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
         "config": {"workload": WORKLOAD, "m": 37810, "m_pad": 37824, "linears_per_step": len(lins),
                    "l2": "every input larger than L2 (129 MB); no flush", "parallelism": f"replicas{world}"},
-        "roofline": {"bound": "tensor", "kernel": f"nvf4_gemm_kernel ({dom.name}: M=37810 N={dom.w.n} K={dom.w.k})",
+        "roofline": {"bound": "tensor",
+                     "kernel": f"{GEMM_KERNELS[args.gemm_kernel]} ({dom.name}: M=37810 N={dom.w.n} K={dom.w.k})",
                      "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(achieved / fp4_peak, 4), "traffic": _profile_traffic(dom.name),
+                     "frac": round(achieved / fp4_peak, 4), "traffic": _profile_traffic(dom.name) if args.gemm_kernel in (0, 4) else None,
                      "peak_source": f"{peaks['source']} bf16 sustained {peaks['bf16_sustained']} TFLOP/s x "
                                     f"{FP4_PER_BF16:g} (nominal NVFP4/BF16 ratio)"},
         "kernels": kernels,
