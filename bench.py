@@ -453,7 +453,7 @@ def main():
     ap.add_argument("--gemm-kernel", type=int, default=0, choices=(0, 1, 2, 3, 4),
                     help="GEMM kernel (h3fp4_gemm_config.cta_pair): 0 library default (4), 1 single CTA, "
                          "2 CTA pair with scale warps, 3 two-CTA cluster with B multicast, "
-                         "4 CTA pair with the scales copied into TMEM by the MMA warp")
+                         "4 CTA pair with the scales copied into TMEM by a copy warp")
     ap.add_argument("--profile-range", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()

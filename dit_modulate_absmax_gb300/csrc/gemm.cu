@@ -72,7 +72,6 @@ constexpr int kScaleWarps = 4;                     // one per TMEM lane quarter
 constexpr int kFirstEpiWarp = 2;
 constexpr int kFirstScaleWarp = kFirstEpiWarp + kEpiWarps;
 constexpr int kThreads = 32 * (2 + kEpiWarps + kScaleWarps);
-constexpr int kThreadsCp = 32 * (2 + kEpiWarps);   // scales copied by the MMA warp: no scale warps
 constexpr int kDefaultNGroup = 28;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
@@ -826,42 +825,79 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace pair
 
 // ---------------------------------------------------------------------------
-// CTA-pair kernel with the scales copied by the MMA warp (cta_group::2
-// tcgen05.cp).  Per K step each CTA loads, into one stage of a 5-stage ring,
-// its 128 rows of A, its 128 rows of B, its A scale atoms and all 256 rows'
-// B scale atoms, every load completing on the leader's full barrier (the
-// cta_group::2 form of the tensor copy; out-of-range boxes, e.g. the absent
-// second row block of the last M tile, are zero-filled and still count their
-// full size).  The leader's MMA warp, warp-collectively, copies the stage's 12
-// scale atoms into both CTAs' TMEM slot for that stage (each CTA's shared
-// memory into its own TMEM), issues the 4 pair MMAs and commits the stage
-// free in both CTAs.  No scale warps and no per-step hand-off between the
-// SMs other than the loads' own completion.  Each CTA's epilogue drains its
-// own 128 accumulator rows; kGated selects the gated residual epilogue.
+// CTA-pair kernel with the scales copied into TMEM by tcgen05.cp
+// (cta_group::2).  Per K step each CTA loads, into one stage of a 5-stage
+// ring, its A scale atoms and all 256 rows' B scale atoms (onto the leader's
+// sf_full barrier), then its 128 rows of A and 128 rows of B (onto the
+// leader's full barrier) -- the cta_group::2 form of the tensor copy;
+// out-of-range boxes, e.g. the absent second row block of the last M tile,
+// are zero-filled and still count their full size.  In the leader, a copy
+// warp waits for a stage's scales and copies its 12 atoms into both CTAs'
+// TMEM slot for the stage (each CTA's shared memory into its own TMEM),
+// committing to sf_ready; the MMA warp waits for sf_ready and full, issues
+// the 4 pair MMAs and commits the stage free in both CTAs.  Both warps run
+// their loops warp-collectively, each tcgen05 instruction issued by one
+// elected lane.  The issuing warp's per-stage time is what the tensor pipe
+// waits on: one warp issuing 12 copies and 4 MMAs per stage kept the pipe
+// ~65 % busy; split over two warps, with the copies overlapping the A/B loads,
+// the same GEMM runs 10 % faster.  No scale warps and no per-step hand-off
+// between the SMs other than the loads' own completion.  Each CTA's epilogue
+// drains its own 128 accumulator rows; kGated selects the gated residual
+// epilogue.
 // ---------------------------------------------------------------------------
 namespace paircp {
 
-constexpr int kStages = 5;
-constexpr uint32_t STAGE_TX = 2 * (pair::A_BYTES + pair::B_BYTES + pair::SFA_BYTES + pair::SFB_BYTES);
+// Stage geometry for kBK K-elements per stage: 256 (128-byte operand rows,
+// 128-byte swizzle, 5 stages; the kernel in use) or 128 (64-byte rows, 64-byte
+// swizzle, 10 stages: the same bytes in flight, each stage held half as long
+// by its MMAs -- measured 35-50 % slower: the per-stage waits and commits
+// double, and the issuing warps' per-stage costs are what the pipe waits on).
+constexpr int kCopyWarp = 2;                        // leader: copies the scale atoms into TMEM
+constexpr int kFirstEpi = 3;                        // epilogue warps 3 .. 10
+constexpr int kThreadsPair = 32 * (kFirstEpi + kEpiWarps);
 
+template <int kBK>
+struct Geo {
+    static constexpr int kStages = kBK == 256 ? 5 : 10;
+    static constexpr int kMmas = kBK / 64;                  // K = 64 per MMA
+    static constexpr uint32_t ROW = kBK / 2;                // bytes of one operand row per stage
+    static constexpr uint32_t A_BYTES = 128 * ROW;          // this CTA's 128 rows of A
+    static constexpr uint32_t B_BYTES = 128 * ROW;          // this CTA's 128 rows of B
+    static constexpr uint32_t SFA_BYTES = kMmas * ATOM;     // this CTA's A scale atoms
+    static constexpr uint32_t SFB_BYTES = 2 * kMmas * ATOM; // all 256 B rows' scale atoms
+    static constexpr uint32_t AB_TX = 2 * (A_BYTES + B_BYTES);        // both CTAs' operands of a stage
+    static constexpr uint32_t SF_TX = 2 * (SFA_BYTES + SFB_BYTES);    // both CTAs' scale atoms of a stage
+    static constexpr uint32_t SF_COLS = 12 * kMmas;         // TMEM columns of one stage's scales
+    static constexpr uint32_t LAYOUT = kBK == 256 ? 2 : 4;  // descriptor swizzle mode: 128 B / 64 B
+    static constexpr uint32_t SBO = 8 * ROW;                // bytes between 8-row core-matrix groups
+    static_assert(SF_COL + kStages * SF_COLS <= TMEM_COLS, "TMEM scale slots");
+};
+
+template <int kBK>
 struct __align__(1024) Smem {
-    uint8_t a[kStages][pair::A_BYTES];
-    uint8_t b[kStages][pair::B_BYTES];
-    uint8_t sfa[kStages][pair::SFA_BYTES];
-    uint8_t sfb[kStages][pair::SFB_BYTES];
+    using G = Geo<kBK>;
+    uint8_t a[G::kStages][G::A_BYTES];
+    uint8_t b[G::kStages][G::B_BYTES];
+    uint8_t sfa[G::kStages][G::SFA_BYTES];
+    uint8_t sfb[G::kStages][G::SFB_BYTES];
     uint8_t cst[kEpiWarps][CST_BYTES];  // per epilogue warp: output staging for tensor stores
     uint64_t res_full[kEpiWarps];       // per epilogue warp: a residual block landed in cst (gated epilogue)
-    uint64_t full[kStages];             // leader: both CTAs' operands and scales landed
-    uint64_t empty[kStages];            // both CTAs, arrived by the leader's commits
+    uint64_t full[G::kStages];          // leader: both CTAs' A and B landed
+    uint64_t sf_full[G::kStages];       // leader: both CTAs' scale atoms landed
+    uint64_t sf_ready[G::kStages];      // leader: the stage's scale atoms are in TMEM (copy warp's commit)
+    uint64_t empty[G::kStages];         // both CTAs, arrived by the leader's commits
     uint64_t acc_full;                  // both CTAs
     uint64_t acc_empty;                 // used in the leader
     uint32_t tmem_base;
 };
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
-static_assert(SF_COL + kStages * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM scale slots");
+template <int kBK>
+constexpr size_t smem_bytes()
+{
+    return sizeof(Smem<kBK>) + 1024;
+}
 
-template <bool kGated>
-__global__ void __launch_bounds__(kThreadsCp, 1)
+template <bool kGated, int kBK>
+__global__ void __launch_bounds__(kThreadsPair, 1)
     nvf4_gemm_pair_cp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
@@ -869,18 +905,22 @@ __global__ void __launch_bounds__(kThreadsCp, 1)
                              const float *__restrict__ b_ts, int m, int n, int k, int m_tiles2, int n_tiles,
                              int n_group)
 {
+    using G = Geo<kBK>;
+    constexpr int kStages = G::kStages;
     extern __shared__ uint8_t smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem<kBK> &sm = *reinterpret_cast<Smem<kBK> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
-    const int kt_count = k / BK;
-    const int chunks_per_rb = k / 256;          // 2 KB scale chunks per 128-row block
+    const int kt_count = k / kBK;
+    const int sf_rows_per_rb = k / 32;          // 256-byte rows of scale atoms per 128-row block
     const int total_tiles = m_tiles2 * n_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.sf_full[s]), 1);
+            mbar_init(smem_u32(&sm.sf_ready[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), 1);
         }
         mbar_init(smem_u32(&sm.acc_full), 1);
@@ -920,20 +960,66 @@ __global__ void __launch_bounds__(kThreadsCp, 1)
                         ok = false;
                         break;
                     }
-                    if (rank == 0)
-                        mbar_arrive_expect_tx(smem_u32(&sm.full[s]), STAGE_TX);
+                    if (rank == 0) {
+                        mbar_arrive_expect_tx(smem_u32(&sm.sf_full[s]), G::SF_TX);
+                        mbar_arrive_expect_tx(smem_u32(&sm.full[s]), G::AB_TX);
+                    }
+                    // scales first, on their own barrier: the copy warp moves them into TMEM
+                    // while A and B are still in flight
+                    const uint32_t sbar = mapa_shared(smem_u32(&sm.sf_full[s]), 0);
+                    constexpr int sf_stage_rows = G::SFA_BYTES / 256;
+                    tma_load_2d_pair(smem_u32(sm.sfa[s]), &tmSFA, 0, rb_a * sf_rows_per_rb + kt * sf_stage_rows, sbar);
+                    tma_load_2d_pair(smem_u32(sm.sfb[s]), &tmSFB, 0, 2 * nt * sf_rows_per_rb + kt * sf_stage_rows, sbar);
+                    tma_load_2d_pair(smem_u32(sm.sfb[s]) + G::SFB_BYTES / 2, &tmSFB, 0,
+                                     (2 * nt + 1) * sf_rows_per_rb + kt * sf_stage_rows, sbar);
                     const uint32_t bar = mapa_shared(smem_u32(&sm.full[s]), 0);
-                    tma_load_2d_pair(smem_u32(sm.sfa[s]), &tmSFA, 0, (rb_a * chunks_per_rb + kt) * 8, bar);
-                    tma_load_2d_pair(smem_u32(sm.sfb[s]), &tmSFB, 0, (2 * nt * chunks_per_rb + kt) * 8, bar);
-                    tma_load_2d_pair(smem_u32(sm.sfb[s]) + pair::SFB_BYTES / 2, &tmSFB, 0,
-                                     ((2 * nt + 1) * chunks_per_rb + kt) * 8, bar);
-                    tma_load_2d_pair(smem_u32(sm.a[s]), &tmA, kt * BKB, mt2 * 256 + static_cast<int>(rank) * 128, bar);
-                    tma_load_2d_pair(smem_u32(sm.b[s]), &tmB, kt * BKB, nt * pair::BN + static_cast<int>(rank) * 128,
+                    tma_load_2d_pair(smem_u32(sm.a[s]), &tmA, kt * G::ROW, mt2 * 256 + static_cast<int>(rank) * 128,
+                                     bar);
+                    tma_load_2d_pair(smem_u32(sm.b[s]), &tmB, kt * G::ROW, nt * pair::BN + static_cast<int>(rank) * 128,
                                      bar);
                 }
             }
         }
+    } else if (warp == kCopyWarp) {
+        // Leader only: per stage, wait until both CTAs' scale atoms landed,
+        // copy them into both CTAs' TMEM slot for the stage (each CTA's shared
+        // memory into its own TMEM) and commit to sf_ready.  A slot is
+        // rewritten only after its stage's scale barrier completed again, i.e.
+        // after the producers saw the commit of the MMAs that last read it.
+        if (rank == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = pair_id; t < total_tiles && ok; t += num_pairs) {
+                for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                    const int s = it % kStages;
+                    if (!warp_wait(smem_u32(&sm.sf_full[s]), (it / kStages) & 1)) {
+                        if (lane == 0)
+                            record_error(ERR_WAIT_SCALES);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + SF_COL + s * G::SF_COLS;
+                    const uint32_t sfb_t = sfa_t + 4 * G::kMmas;
+                    const uint32_t sfa_s = smem_u32(sm.sfa[s]), sfb_s = smem_u32(sm.sfb[s]);
+#pragma unroll
+                    for (int j = 0; j < G::kMmas; ++j) {
+                        tc_cp_32x128b_warpx4_pair_elect(sfa_t + 4 * j, smem_desc(sfa_s + j * ATOM, 0, 128, 0));
+                        tc_cp_32x128b_warpx4_pair_elect(sfb_t + 8 * j, smem_desc(sfb_s + j * ATOM, 0, 128, 0));
+                        tc_cp_32x128b_warpx4_pair_elect(sfb_t + 8 * j + 4,
+                                                        smem_desc(sfb_s + G::SFB_BYTES / 2 + j * ATOM, 0, 128, 0));
+                    }
+                    tc_commit_pair_mc_elect(smem_u32(&sm.sf_ready[s]), 0x1);
+                }
+            }
+        }
     } else if (warp == 1) {
+        // Leader only: per stage, wait for sf_ready (the scales are in TMEM)
+        // and full (A and B landed), issue the pair MMAs and commit the stage
+        // free in both CTAs.  With the scale copies in their own warp this
+        // warp issues 5 tcgen05 instructions per stage instead of 17: its
+        // per-stage issue time, which the tensor pipe otherwise waits on,
+        // drops well below the MMAs' own time.
         if (rank == 0) {
             constexpr uint32_t idesc = idesc_nvf4(2 * pair::BM, pair::BN);
             uint32_t it = 0, local = 0;
@@ -947,27 +1033,20 @@ __global__ void __launch_bounds__(kThreadsCp, 1)
                 tc_fence_after();
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
-                    if (!warp_wait(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
+                    if (!warp_wait(smem_u32(&sm.sf_ready[s]), (it / kStages) & 1) ||
+                        !warp_wait(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
                         if (lane == 0)
                             record_error(ERR_WAIT_FULL);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem + SF_COL + s * SF_COLS_PER_STAGE;
-                    const uint32_t sfb_t = sfa_t + 16;
-                    const uint32_t sfa_s = smem_u32(sm.sfa[s]), sfb_s = smem_u32(sm.sfb[s]);
+                    const uint32_t sfa_t = tmem + SF_COL + s * G::SF_COLS;
+                    const uint32_t sfb_t = sfa_t + 4 * G::kMmas;
+                    const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, G::SBO, G::LAYOUT);
+                    const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, G::SBO, G::LAYOUT);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        tc_cp_32x128b_warpx4_pair_elect(sfa_t + 4 * j, smem_desc(sfa_s + j * ATOM, 0, 128, 0));
-                        tc_cp_32x128b_warpx4_pair_elect(sfb_t + 8 * j, smem_desc(sfb_s + j * ATOM, 0, 128, 0));
-                        tc_cp_32x128b_warpx4_pair_elect(sfb_t + 8 * j + 4,
-                                                        smem_desc(sfb_s + pair::SFB_BYTES / 2 + j * ATOM, 0, 128, 0));
-                    }
-                    const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, 1024, 2);
-                    const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, 1024, 2);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
+                    for (int j = 0; j < G::kMmas; ++j)
                         tc_mma_nvf4_pair_elect(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, idesc, sfa_t + 4 * j,
                                                sfb_t + 8 * j, (kt | j) != 0);
                     tc_commit_pair_mc_elect(smem_u32(&sm.empty[s]), 0x3);
@@ -978,7 +1057,7 @@ __global__ void __launch_bounds__(kThreadsCp, 1)
         }
     } else {
         const int q = warp & 3;
-        const int half = (warp - kFirstEpiWarp) >> 2;
+        const int half = (warp - kFirstEpi) >> 2;
         const float alpha = __fmul_rn(*a_ts, *b_ts);
         const uint32_t leader_acc_empty = mapa_shared(smem_u32(&sm.acc_empty), 0);
         uint32_t local = 0, rphase = 0;
@@ -1012,15 +1091,15 @@ __global__ void __launch_bounds__(kThreadsCp, 1)
                 mbar_arrive_cluster_relaxed(leader_acc_empty);
             const int row0 = mt2 * 256 + static_cast<int>(rank) * pair::BM + q * 32;
             if (kGated) {
-                if (!store_rows_gated(&tmC, &tmR, smem_u32(sm.cst[warp - kFirstEpiWarp]),
-                                      smem_u32(&sm.res_full[warp - kFirstEpiWarp]), rphase, pk,
+                if (!store_rows_gated(&tmC, &tmR, smem_u32(sm.cst[warp - kFirstEpi]),
+                                      smem_u32(&sm.res_full[warp - kFirstEpi]), rphase, pk,
                                       nt * pair::BN + half * 128, row0, lane, gate_row(ge, row0 + lane))) {
                     if (lane == 0)
                         record_error(ERR_WAIT_ACC);
                     break;
                 }
             } else {
-                store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpiWarp]), pk, nt * pair::BN + half * 128, row0, lane);
+                store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpi]), pk, nt * pair::BN + half * 128, row0, lane);
             }
         }
         if (lane == 0)
@@ -1055,18 +1134,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 // 2-D uint8 tensor map over a K-major packed operand [rows, k/2] with a box of
 // 128 bytes x box_rows and 128-byte swizzle (rows past `rows` read as zero).
-bool make_operand_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t kbytes, uint32_t box_rows)
+bool make_operand_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t kbytes, uint32_t box_rows,
+                      uint32_t box_kbytes = BKB)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kbytes)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BKB), box_rows};
+    cuuint32_t box[2] = {box_kbytes, box_rows};
     cuuint32_t estr[2] = {1, 1};
+    // 128-byte rows use the 128-byte swizzle, 64-byte rows the 64-byte one (the MMA descriptors match)
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, box_kbytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -1089,14 +1170,14 @@ bool make_output_map(CUtensorMap *tm, void *base, int64_t m, int64_t n, int64_t 
 
 // 2-D uint8 tensor map viewing a scale buffer of `bytes` bytes as rows of 256
 // bytes, box 256 x 8 (one 2 KB chunk = 4 scale atoms), no swizzle.
-bool make_scale_map(CUtensorMap *tm, const void *base, int64_t bytes)
+bool make_scale_map(CUtensorMap *tm, const void *base, int64_t bytes, uint32_t box_rows = 8)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(pair::SF_ROW), static_cast<cuuint64_t>(bytes / pair::SF_ROW)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(pair::SF_ROW)};
-    cuuint32_t box[2] = {pair::SF_ROW, 8};
+    cuuint32_t box[2] = {pair::SF_ROW, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1230,7 +1311,7 @@ bool make_gated(const GatedArgs *gated, const CUtensorMap &tmC, int64_t m, int64
     return true;
 }
 
-template <bool kGated>
+template <bool kGated, int kBK>
 cudaError_t set_pair_cp_smem()
 {
     static bool attr_set[64] = {false};
@@ -1239,8 +1320,9 @@ cudaError_t set_pair_cp_smem()
     if (e != cudaSuccess)
         return e;
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(paircp::nvf4_gemm_pair_cp_kernel<kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(paircp::kSmemBytes));
+        e = cudaFuncSetAttribute(paircp::nvf4_gemm_pair_cp_kernel<kGated, kBK>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(paircp::smem_bytes<kBK>()));
         if (e != cudaSuccess)
             return e;
         attr_set[dev] = true;
@@ -1248,19 +1330,23 @@ cudaError_t set_pair_cp_smem()
     return cudaSuccess;
 }
 
+template <int kBK>
 h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
                             const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m,
                             int64_t m_pad, int64_t n, int64_t k, int n_group_cfg, const GatedArgs *gated,
                             cudaStream_t st)
 {
+    using G = paircp::Geo<kBK>;
     const int64_t sfa_rows = (m_pad + 127) / 128 * 128, sfb_rows = (n + 127) / 128 * 128;
     CUtensorMap tmA, tmB, tmSFA, tmSFB, tmC, tmR;
     GatedEpilogue ge;
-    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, pair::BM) || !make_operand_map(&tmB, b_q, n, k / 2, 128) ||
-        !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16)) || !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16)) ||
+    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, pair::BM, G::ROW) ||
+        !make_operand_map(&tmB, b_q, n, k / 2, 128, G::ROW) ||
+        !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16), G::SFA_BYTES / 256) ||
+        !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16), G::SFA_BYTES / 256) ||
         !make_output_map(&tmC, c, m, n, ldc) || !make_gated(gated, tmC, m, n, &tmR, &ge))
         return H3FP4_ERR_CUDA;
-    if ((gated ? set_pair_cp_smem<true>() : set_pair_cp_smem<false>()) != cudaSuccess)
+    if ((gated ? set_pair_cp_smem<true, kBK>() : set_pair_cp_smem<false, kBK>()) != cudaSuccess)
         return H3FP4_ERR_CUDA;
     const int m_tiles2 = static_cast<int>((m + 255) / 256);
     const int n_tiles = static_cast<int>((n + pair::BN - 1) / pair::BN);
@@ -1274,8 +1360,8 @@ h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float
     const int pairs = static_cast<int>(total < max_pairs ? total : max_pairs);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(2 * pairs, 1, 1);
-    lc.blockDim = dim3(kThreadsCp, 1, 1);
-    lc.dynamicSmemBytes = paircp::kSmemBytes;
+    lc.blockDim = dim3(paircp::kThreadsPair, 1, 1);
+    lc.dynamicSmemBytes = paircp::smem_bytes<kBK>();
     lc.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1285,10 +1371,10 @@ h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float
     lc.attrs = attr;
     lc.numAttrs = 1;
     const cudaError_t e =
-        gated ? cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<true>, tmA, tmB, tmSFA, tmSFB, tmC, tmR, ge,
-                                   a_ts, b_ts, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), m_tiles2,
-                                   n_tiles, n_group)
-              : cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<false>, tmA, tmB, tmSFA, tmSFB, tmC, tmR, ge,
+        gated ? cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<true, kBK>, tmA, tmB, tmSFA, tmSFB, tmC, tmR,
+                                   ge, a_ts, b_ts, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k),
+                                   m_tiles2, n_tiles, n_group)
+              : cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<false, kBK>, tmA, tmB, tmSFA, tmSFB, tmC, tmR, ge,
                                    a_ts, b_ts, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), m_tiles2,
                                    n_tiles, n_group);
     return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
@@ -1301,7 +1387,7 @@ h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a
     if (m == 0 || n == 0)
         return H3FP4_OK;
     if (cfg.cta_pair == 0 || cfg.cta_pair == 4)   // the default: measured fastest in the DiT step
-        return launch_pair_cp(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, gated, st);
+        return launch_pair_cp<256>(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, gated, st);
     if (cfg.cta_pair == 2) {
         if (gated != nullptr)
             return H3FP4_ERR_UNSUPPORTED;

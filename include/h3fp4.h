@@ -192,8 +192,9 @@ typedef struct h3fp4_gemm_config {
      * A and half of B; 6-stage ring; scale warps; no gated epilogue), 3 =
      * clusters of two CTAs on the two 128 x 256 tiles of one 256 x 256 block,
      * each loading its own A and half of the shared B tile, multicast into
-     * both (4-stage ring, scale warps), 4 = CTA pairs as 2 whose MMA warp
-     * copies the scales into TMEM itself (tcgen05.cp; 5-stage ring). */
+     * both (4-stage ring, scale warps), 4 = CTA pairs as 2 whose leader
+     * copies the scales into TMEM with tcgen05.cp from a warp of its own
+     * (5-stage ring). */
     int32_t cta_pair;
     int32_t reserved;  /* must be 0 */
 } h3fp4_gemm_config;
