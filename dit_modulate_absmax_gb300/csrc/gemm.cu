@@ -831,19 +831,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // sf_full barrier), then its 128 rows of A and 128 rows of B (onto the
 // leader's full barrier) -- the cta_group::2 form of the tensor copy;
 // out-of-range boxes, e.g. the absent second row block of the last M tile,
-// are zero-filled and still count their full size.  In the leader, a copy
-// warp waits for a stage's scales and copies its 12 atoms into both CTAs'
-// TMEM slot for the stage (each CTA's shared memory into its own TMEM),
-// committing to sf_ready; the MMA warp waits for sf_ready and full, issues
-// the 4 pair MMAs and commits the stage free in both CTAs.  Both warps run
-// their loops warp-collectively, each tcgen05 instruction issued by one
-// elected lane.  The issuing warp's per-stage time is what the tensor pipe
-// waits on: one warp issuing 12 copies and 4 MMAs per stage kept the pipe
-// ~65 % busy; split over two warps, with the copies overlapping the A/B loads,
-// the same GEMM runs 10 % faster.  No scale warps and no per-step hand-off
-// between the SMs other than the loads' own completion.  Each CTA's epilogue
-// drains its own 128 accumulator rows; kGated selects the gated residual
-// epilogue.
+// are zero-filled and still count their full size.  In the leader, two copy
+// warps wait for a stage's scales and copy its 12 atoms (6 each) into both
+// CTAs' TMEM slot for the stage (each CTA's shared memory into its own TMEM),
+// each committing to sf_ready; the MMA warp waits for sf_ready and full,
+// issues the 4 pair MMAs and commits the stage free in both CTAs.  These
+// warps run their loops warp-collectively, each tcgen05 instruction issued by
+// one elected lane.  What the tensor pipe waits on is the issuing warps'
+// per-stage time (a satisfied barrier wait alone costs ~100 cycles, a tcgen05
+// instruction ~30): one warp issuing 12 copies and 4 MMAs per stage kept the
+// pipe ~65 % busy; with the copies in two warps of their own, overlapping the
+// A/B loads, the same GEMM runs 12 % faster.  No scale warps and no per-step
+// hand-off between the SMs other than the loads' own completion.  Each CTA's
+// epilogue drains its own 128 accumulator rows; kGated selects the gated
+// residual epilogue.
 // ---------------------------------------------------------------------------
 namespace paircp {
 
@@ -852,8 +853,9 @@ namespace paircp {
 // swizzle, 10 stages: the same bytes in flight, each stage held half as long
 // by its MMAs -- measured 35-50 % slower: the per-stage waits and commits
 // double, and the issuing warps' per-stage costs are what the pipe waits on).
-constexpr int kCopyWarp = 2;                        // leader: copies the scale atoms into TMEM
-constexpr int kFirstEpi = 3;                        // epilogue warps 3 .. 10
+constexpr int kFirstCopyWarp = 2;                   // leader: warps 2 and 3 copy the scale atoms into TMEM
+constexpr int kCopyWarps = 2;
+constexpr int kFirstEpi = kFirstCopyWarp + kCopyWarps;   // epilogue warps 4 .. 11
 constexpr int kThreadsPair = 32 * (kFirstEpi + kEpiWarps);
 
 template <int kBK>
@@ -920,7 +922,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.sf_full[s]), 1);
-            mbar_init(smem_u32(&sm.sf_ready[s]), 1);
+            mbar_init(smem_u32(&sm.sf_ready[s]), kCopyWarps);
             mbar_init(smem_u32(&sm.empty[s]), 1);
         }
         mbar_init(smem_u32(&sm.acc_full), 1);
@@ -980,12 +982,15 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 }
             }
         }
-    } else if (warp == kCopyWarp) {
+    } else if (warp >= kFirstCopyWarp && warp < kFirstEpi) {
         // Leader only: per stage, wait until both CTAs' scale atoms landed,
         // copy them into both CTAs' TMEM slot for the stage (each CTA's shared
-        // memory into its own TMEM) and commit to sf_ready.  A slot is
+        // memory into its own TMEM) and commit to sf_ready.  The two copy
+        // warps split the stage's MMAs between them (6 copies each).  A slot is
         // rewritten only after its stage's scale barrier completed again, i.e.
         // after the producers saw the commit of the MMAs that last read it.
+        constexpr int kPerWarp = G::kMmas / kCopyWarps;
+        const int j0 = (warp - kFirstCopyWarp) * kPerWarp;
         if (rank == 0) {
             uint32_t it = 0;
             bool ok = true;
@@ -1003,7 +1008,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                     const uint32_t sfb_t = sfa_t + 4 * G::kMmas;
                     const uint32_t sfa_s = smem_u32(sm.sfa[s]), sfb_s = smem_u32(sm.sfb[s]);
 #pragma unroll
-                    for (int j = 0; j < G::kMmas; ++j) {
+                    for (int j = j0; j < j0 + kPerWarp; ++j) {
                         tc_cp_32x128b_warpx4_pair_elect(sfa_t + 4 * j, smem_desc(sfa_s + j * ATOM, 0, 128, 0));
                         tc_cp_32x128b_warpx4_pair_elect(sfb_t + 8 * j, smem_desc(sfb_s + j * ATOM, 0, 128, 0));
                         tc_cp_32x128b_warpx4_pair_elect(sfb_t + 8 * j + 4,
