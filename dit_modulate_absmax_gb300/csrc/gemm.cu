@@ -834,8 +834,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // are zero-filled and still count their full size.  In the leader, two copy
 // warps wait for a stage's scales and copy its 12 atoms (6 each) into both
 // CTAs' TMEM slot for the stage (each CTA's shared memory into its own TMEM),
-// each committing to sf_ready; the MMA warp waits for sf_ready and full,
-// issues the 4 pair MMAs and commits the stage free in both CTAs.  These
+// each committing to the same full barrier, which therefore completes once
+// A and B have landed and the scales are in TMEM (3 arrivals: the producer's
+// expect-tx and the two commits); the MMA warp waits for it, issues the 4
+// pair MMAs and commits the stage free in both CTAs.  These
 // warps run their loops warp-collectively, each tcgen05 instruction issued by
 // one elected lane.  What the tensor pipe waits on is the issuing warps'
 // per-stage time (a satisfied barrier wait alone costs ~100 cycles, a tcgen05
@@ -884,9 +886,8 @@ struct __align__(1024) Smem {
     uint8_t sfb[G::kStages][G::SFB_BYTES];
     uint8_t cst[kEpiWarps][CST_BYTES];  // per epilogue warp: output staging for tensor stores
     uint64_t res_full[kEpiWarps];       // per epilogue warp: a residual block landed in cst (gated epilogue)
-    uint64_t full[G::kStages];          // leader: both CTAs' A and B landed
+    uint64_t full[G::kStages];          // leader: both CTAs' A and B landed and the copy warps' commits arrived
     uint64_t sf_full[G::kStages];       // leader: both CTAs' scale atoms landed
-    uint64_t sf_ready[G::kStages];      // leader: the stage's scale atoms are in TMEM (copy warp's commit)
     uint64_t empty[G::kStages];         // both CTAs, arrived by the leader's commits
     uint64_t acc_full;                  // both CTAs
     uint64_t acc_empty;                 // used in the leader
@@ -920,9 +921,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&sm.full[s]), 1);
+            // the producer's expect-tx arrival plus one commit per copy warp (scales in TMEM)
+            mbar_init(smem_u32(&sm.full[s]), 1 + kCopyWarps);
             mbar_init(smem_u32(&sm.sf_full[s]), 1);
-            mbar_init(smem_u32(&sm.sf_ready[s]), kCopyWarps);
             mbar_init(smem_u32(&sm.empty[s]), 1);
         }
         mbar_init(smem_u32(&sm.acc_full), 1);
@@ -1014,7 +1015,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                         tc_cp_32x128b_warpx4_pair_elect(sfb_t + 8 * j + 4,
                                                         smem_desc(sfb_s + G::SFB_BYTES / 2 + j * ATOM, 0, 128, 0));
                     }
-                    tc_commit_pair_mc_elect(smem_u32(&sm.sf_ready[s]), 0x1);
+                    tc_commit_pair_mc_elect(smem_u32(&sm.full[s]), 0x1);
                 }
             }
         }
@@ -1038,8 +1039,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 tc_fence_after();
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
-                    if (!warp_wait(smem_u32(&sm.sf_ready[s]), (it / kStages) & 1) ||
-                        !warp_wait(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
+                    if (!warp_wait(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
                         if (lane == 0)
                             record_error(ERR_WAIT_FULL);
                         ok = false;
