@@ -1335,6 +1335,18 @@ cudaError_t set_pair_cp_smem()
     return cudaSuccess;
 }
 
+// Default N-group of the CTA-pair kernel: the fewest near-equal groups of
+// N-tiles whose B tiles (256 rows x k/2 bytes each) stay within ~27.5 MB, the
+// set that must stay L2-resident while a group sweeps all M tiles.  Measured
+// at 37,810 rows: k = 7,168 -> 28 of 84 or 56 tiles, k = 14,336 -> 14 of 28
+// (8 % faster than 28) and 11 of 21, k = 5,376 -> 28 of 84.
+int pair_default_n_group(int n_tiles, int64_t k)
+{
+    const int64_t target = 27500000 / (128 * k) > 1 ? 27500000 / (128 * k) : 1;
+    const int64_t groups = (n_tiles + target - 1) / target;
+    return static_cast<int>((n_tiles + groups - 1) / groups);
+}
+
 template <int kBK>
 h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
                             const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m,
@@ -1358,7 +1370,7 @@ h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float
     const int64_t total = static_cast<int64_t>(m_tiles2) * n_tiles;
     if (total > 0x7FFFFFFF)
         return H3FP4_ERR_SHAPE;
-    int n_group = n_group_cfg > 0 ? n_group_cfg : kDefaultNGroup;
+    int n_group = n_group_cfg > 0 ? n_group_cfg : pair_default_n_group(n_tiles, k);
     if (n_group > n_tiles)
         n_group = n_tiles;
     const int max_pairs = sm_count() / 2;

@@ -179,11 +179,12 @@ H3FP4_API h3fp4_status h3fp4_quantize_pack(const void *x_bf16, int64_t ldx, int6
 
 /* Tuning knobs of the GEMM; pass NULL for the defaults. */
 typedef struct h3fp4_gemm_config {
-    /* N-group A-tile reuse factor: the persistent schedule walks the 128 x 256
-     * output tiles in groups of n_group N-tiles x all M-tiles, N fastest, so
-     * each 128-row A tile serves n_group consecutive output tiles while it is
-     * L2-resident (0 = default 28; values above the number of N-tiles are
-     * clamped). */
+    /* N-group A-tile reuse factor: the persistent schedule walks the output
+     * tiles (256 columns wide) in groups of n_group N-tiles x all M-tiles, N
+     * fastest, so each A row block serves n_group consecutive output tiles
+     * while it is L2-resident (0 = kernel default: the default kernel takes
+     * the fewest near-equal groups whose B tiles total at most ~27.5 MB, the
+     * others 28; values above the number of N-tiles are clamped). */
     int32_t n_group;
     int32_t stages;    /* reserved, must be 0 (the pipeline depth is fixed per kernel) */
     /* GEMM kernel: 0 = library default (currently 4), 1 = one CTA per 128 x 256 output tile
