@@ -124,6 +124,21 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
+// As warp_wait, but polling with the non-blocking test_wait instead of a
+// suspending try_wait: for a warp whose wake-up latency sits on the critical
+// path (the default GEMM's MMA warp: 1.2 % faster), at the price of issue
+// slots while it spins.  Bounded like every other wait.
+__device__ __forceinline__ bool warp_wait_spin(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (__all_sync(0xFFFFFFFFu, mbar_test_wait(bar, parity)))
+            return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
 // The scale layout the block-scaled MMA reads from TMEM: for MMA K step j,
 // row i (16 bytes) of the 128x4 atom goes to columns 4j .. 4j+3 of lane
 // 32q + i for every lane quarter q, i.e. the layout of a tcgen05.cp
@@ -1039,7 +1054,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 tc_fence_after();
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
-                    if (!warp_wait(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
+                    if (!warp_wait_spin(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
                         if (lane == 0)
                             record_error(ERR_WAIT_FULL);
                         ok = false;
