@@ -865,21 +865,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 namespace paircp {
 
-// Stage geometry for kBK K-elements per stage: 256 (128-byte operand rows,
-// 128-byte swizzle, 5 stages; the kernel in use) or 128 (64-byte rows, 64-byte
-// swizzle, 10 stages: the same bytes in flight, each stage held half as long
-// by its MMAs -- measured 35-50 % slower: the per-stage waits and commits
-// double, and the issuing warps' per-stage costs are what the pipe waits on).
 constexpr int kFirstCopyWarp = 2;                   // leader: warps 2 and 3 copy the scale atoms into TMEM
 constexpr int kCopyWarps = 2;
 constexpr int kFirstEpi = kFirstCopyWarp + kCopyWarps;   // epilogue warps 4 .. 11
 constexpr int kThreadsPair = 32 * (kFirstEpi + kEpiWarps);
 
-template <int kBK>
+// Stage geometry: BK = 256 K-elements per stage (128-byte operand rows with the
+// 128-byte swizzle), 5 stages.  (Stages of K = 128 -- 64-byte rows, 10 stages,
+// the same bytes in flight -- measured 35-50 % slower: the per-stage waits and
+// commits double, and the issuing warps' per-stage costs are what the pipe
+// waits on.)
 struct Geo {
-    static constexpr int kStages = kBK == 256 ? 5 : 10;
-    static constexpr int kMmas = kBK / 64;                  // K = 64 per MMA
-    static constexpr uint32_t ROW = kBK / 2;                // bytes of one operand row per stage
+    static constexpr int kStages = 5;
+    static constexpr int kMmas = BK / 64;                   // K = 64 per MMA
+    static constexpr uint32_t ROW = BKB;                    // bytes of one operand row per stage
     static constexpr uint32_t A_BYTES = 128 * ROW;          // this CTA's 128 rows of A
     static constexpr uint32_t B_BYTES = 128 * ROW;          // this CTA's 128 rows of B
     static constexpr uint32_t SFA_BYTES = kMmas * ATOM;     // this CTA's A scale atoms
@@ -887,14 +886,13 @@ struct Geo {
     static constexpr uint32_t AB_TX = 2 * (A_BYTES + B_BYTES);        // both CTAs' operands of a stage
     static constexpr uint32_t SF_TX = 2 * (SFA_BYTES + SFB_BYTES);    // both CTAs' scale atoms of a stage
     static constexpr uint32_t SF_COLS = 12 * kMmas;         // TMEM columns of one stage's scales
-    static constexpr uint32_t LAYOUT = kBK == 256 ? 2 : 4;  // descriptor swizzle mode: 128 B / 64 B
+    static constexpr uint32_t LAYOUT = 2;                   // descriptor swizzle mode: 128 B
     static constexpr uint32_t SBO = 8 * ROW;                // bytes between 8-row core-matrix groups
     static_assert(SF_COL + kStages * SF_COLS <= TMEM_COLS, "TMEM scale slots");
 };
 
-template <int kBK>
 struct __align__(1024) Smem {
-    using G = Geo<kBK>;
+    using G = Geo;
     uint8_t a[G::kStages][G::A_BYTES];
     uint8_t b[G::kStages][G::B_BYTES];
     uint8_t sfa[G::kStages][G::SFA_BYTES];
@@ -908,13 +906,9 @@ struct __align__(1024) Smem {
     uint64_t acc_empty;                 // used in the leader
     uint32_t tmem_base;
 };
-template <int kBK>
-constexpr size_t smem_bytes()
-{
-    return sizeof(Smem<kBK>) + 1024;
-}
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
-template <bool kGated, int kBK>
+template <bool kGated>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     nvf4_gemm_pair_cp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -923,14 +917,14 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                              const float *__restrict__ b_ts, int m, int n, int k, int m_tiles2, int n_tiles,
                              int n_group)
 {
-    using G = Geo<kBK>;
+    using G = Geo;
     constexpr int kStages = G::kStages;
     extern __shared__ uint8_t smem_raw[];
-    Smem<kBK> &sm = *reinterpret_cast<Smem<kBK> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
-    const int kt_count = k / kBK;
+    const int kt_count = k / BK;
     const int sf_rows_per_rb = k / 32;          // 256-byte rows of scale atoms per 128-row block
     const int total_tiles = m_tiles2 * n_tiles;
 
@@ -1154,20 +1148,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 // 2-D uint8 tensor map over a K-major packed operand [rows, k/2] with a box of
 // 128 bytes x box_rows and 128-byte swizzle (rows past `rows` read as zero).
-bool make_operand_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t kbytes, uint32_t box_rows,
-                      uint32_t box_kbytes = BKB)
+bool make_operand_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t kbytes, uint32_t box_rows)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kbytes)};
-    cuuint32_t box[2] = {box_kbytes, box_rows};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BKB), box_rows};
     cuuint32_t estr[2] = {1, 1};
-    // 128-byte rows use the 128-byte swizzle, 64-byte rows the 64-byte one (the MMA descriptors match)
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, box_kbytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -1190,14 +1182,14 @@ bool make_output_map(CUtensorMap *tm, void *base, int64_t m, int64_t n, int64_t 
 
 // 2-D uint8 tensor map viewing a scale buffer of `bytes` bytes as rows of 256
 // bytes, box 256 x 8 (one 2 KB chunk = 4 scale atoms), no swizzle.
-bool make_scale_map(CUtensorMap *tm, const void *base, int64_t bytes, uint32_t box_rows = 8)
+bool make_scale_map(CUtensorMap *tm, const void *base, int64_t bytes)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(pair::SF_ROW), static_cast<cuuint64_t>(bytes / pair::SF_ROW)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(pair::SF_ROW)};
-    cuuint32_t box[2] = {pair::SF_ROW, box_rows};
+    cuuint32_t box[2] = {pair::SF_ROW, 8};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1331,7 +1323,7 @@ bool make_gated(const GatedArgs *gated, const CUtensorMap &tmC, int64_t m, int64
     return true;
 }
 
-template <bool kGated, int kBK>
+template <bool kGated>
 cudaError_t set_pair_cp_smem()
 {
     static bool attr_set[64] = {false};
@@ -1340,9 +1332,8 @@ cudaError_t set_pair_cp_smem()
     if (e != cudaSuccess)
         return e;
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(paircp::nvf4_gemm_pair_cp_kernel<kGated, kBK>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(paircp::smem_bytes<kBK>()));
+        e = cudaFuncSetAttribute(paircp::nvf4_gemm_pair_cp_kernel<kGated>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(paircp::kSmemBytes));
         if (e != cudaSuccess)
             return e;
         attr_set[dev] = true;
@@ -1362,23 +1353,19 @@ int pair_default_n_group(int n_tiles, int64_t k)
     return static_cast<int>((n_tiles + groups - 1) / groups);
 }
 
-template <int kBK>
 h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
                             const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m,
                             int64_t m_pad, int64_t n, int64_t k, int n_group_cfg, const GatedArgs *gated,
                             cudaStream_t st)
 {
-    using G = paircp::Geo<kBK>;
     const int64_t sfa_rows = (m_pad + 127) / 128 * 128, sfb_rows = (n + 127) / 128 * 128;
     CUtensorMap tmA, tmB, tmSFA, tmSFB, tmC, tmR;
     GatedEpilogue ge;
-    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, pair::BM, G::ROW) ||
-        !make_operand_map(&tmB, b_q, n, k / 2, 128, G::ROW) ||
-        !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16), G::SFA_BYTES / 256) ||
-        !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16), G::SFA_BYTES / 256) ||
+    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, pair::BM) || !make_operand_map(&tmB, b_q, n, k / 2, 128) ||
+        !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16)) || !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16)) ||
         !make_output_map(&tmC, c, m, n, ldc) || !make_gated(gated, tmC, m, n, &tmR, &ge))
         return H3FP4_ERR_CUDA;
-    if ((gated ? set_pair_cp_smem<true, kBK>() : set_pair_cp_smem<false, kBK>()) != cudaSuccess)
+    if ((gated ? set_pair_cp_smem<true>() : set_pair_cp_smem<false>()) != cudaSuccess)
         return H3FP4_ERR_CUDA;
     const int m_tiles2 = static_cast<int>((m + 255) / 256);
     const int n_tiles = static_cast<int>((n + pair::BN - 1) / pair::BN);
@@ -1393,7 +1380,7 @@ h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(2 * pairs, 1, 1);
     lc.blockDim = dim3(paircp::kThreadsPair, 1, 1);
-    lc.dynamicSmemBytes = paircp::smem_bytes<kBK>();
+    lc.dynamicSmemBytes = paircp::kSmemBytes;
     lc.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1403,10 +1390,10 @@ h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float
     lc.attrs = attr;
     lc.numAttrs = 1;
     const cudaError_t e =
-        gated ? cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<true, kBK>, tmA, tmB, tmSFA, tmSFB, tmC, tmR,
+        gated ? cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<true>, tmA, tmB, tmSFA, tmSFB, tmC, tmR,
                                    ge, a_ts, b_ts, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k),
                                    m_tiles2, n_tiles, n_group)
-              : cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<false, kBK>, tmA, tmB, tmSFA, tmSFB, tmC, tmR, ge,
+              : cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<false>, tmA, tmB, tmSFA, tmSFB, tmC, tmR, ge,
                                    a_ts, b_ts, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), m_tiles2,
                                    n_tiles, n_group);
     return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
@@ -1419,7 +1406,7 @@ h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a
     if (m == 0 || n == 0)
         return H3FP4_OK;
     if (cfg.cta_pair == 0 || cfg.cta_pair == 4)   // the default: measured fastest in the DiT step
-        return launch_pair_cp<256>(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, gated, st);
+        return launch_pair_cp(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, gated, st);
     if (cfg.cta_pair == 2) {
         if (gated != nullptr)
             return H3FP4_ERR_UNSUPPORTED;
