@@ -1037,8 +1037,11 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         // drops well below the MMAs' own time.
         if (rank == 0) {
             constexpr uint32_t idesc = idesc_nvf4(2 * pair::BM, pair::BN);
+            const int my_tiles = pair_id < total_tiles ? (total_tiles - pair_id + num_pairs - 1) / num_pairs : 0;
+            const uint32_t total_steps = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(kt_count);
             uint32_t it = 0, local = 0;
             bool ok = true;
+            bool known_ready = false;   // the current stage's barrier was seen complete during the previous stage
             for (int t = pair_id; t < total_tiles && ok; t += num_pairs, ++local) {
                 if (!warp_wait(smem_u32(&sm.acc_empty), (local & 1) ^ 1u)) {
                     if (lane == 0)
@@ -1048,7 +1051,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 tc_fence_after();
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
-                    if (!warp_wait_spin(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
+                    if (!known_ready && !warp_wait_spin(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
                         if (lane == 0)
                             record_error(ERR_WAIT_FULL);
                         ok = false;
@@ -1060,9 +1063,19 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                     const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, G::SBO, G::LAYOUT);
                     const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, G::SBO, G::LAYOUT);
 #pragma unroll
-                    for (int j = 0; j < G::kMmas; ++j)
+                    for (int j = 0; j < G::kMmas - 1; ++j)
                         tc_mma_nvf4_pair_elect(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, idesc, sfa_t + 4 * j,
                                                sfb_t + 8 * j, (kt | j) != 0);
+                    // While this stage's MMAs run, look (without waiting) whether the next
+                    // stage is already complete; if so the next iteration skips its wait,
+                    // whose latency otherwise lands between two stages' MMAs.
+                    const uint32_t nx = it + 1;
+                    known_ready = nx < total_steps &&
+                                  __all_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&sm.full[nx % kStages]),
+                                                                         (nx / kStages) & 1));
+                    constexpr int jl = G::kMmas - 1;
+                    tc_mma_nvf4_pair_elect(tmem + ACC_COL, a_desc + 2 * jl, b_desc + 2 * jl, idesc, sfa_t + 4 * jl,
+                                           sfb_t + 8 * jl, 1u);
                     tc_commit_pair_mc_elect(smem_u32(&sm.empty[s]), 0x3);
                 }
                 if (ok)
