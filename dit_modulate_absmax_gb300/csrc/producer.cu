@@ -431,17 +431,17 @@ __device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
     uint32_t out[2];
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {   // 8 values (4 words) at a time
-        uint32_t lo = 0, diff = 0;         // nibble e of diff: the two conversions of value e differ
+        float2 ql[4], qh[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t w = y[4 * hlf + i];
             const float2 a = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-            const float2 ql = __fmul2_rn(a, rl2), qh = __fmul2_rn(a, rh2);
-            const uint32_t b_lo = cvt_e2m1x2(ql.y, ql.x);
-            const uint32_t b_hi = cvt_e2m1x2(qh.y, qh.x);
-            diff |= (b_lo ^ b_hi) << (8 * i);
-            lo |= b_lo << (8 * i);
+            ql[i] = __fmul2_rn(a, rl2);
+            qh[i] = __fmul2_rn(a, rh2);
         }
+        uint32_t lo = cvt_e2m1x8(ql[0], ql[1], ql[2], ql[3]);
+        // nibble e of diff: the two conversions of value e differ
+        uint32_t diff = lo ^ cvt_e2m1x8(qh[0], qh[1], qh[2], qh[3]);
         if (!normal_range) {   // sc or 1/sc outside the normal range: every value by the IEEE division
             lo = 0;
 #pragma unroll

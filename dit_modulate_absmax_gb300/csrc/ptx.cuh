@@ -494,6 +494,22 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float v)
     return r & 0xFFu;
 }
 
+// Four bytes, one per pair: byte i holds the E2M1 code of q_i.x in bits 0-3
+// and of q_i.y in bits 4-7 (the four conversions packed with one mov).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float2 q0, float2 q1, float2 q2, float2 q3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+        : "=r"(r)
+        : "f"(q0.x), "f"(q0.y), "f"(q1.x), "f"(q1.y), "f"(q2.x), "f"(q2.y), "f"(q3.x), "f"(q3.y));
+    return r;
+}
+
 // One byte: E2M1 code of `lo` in bits 0-3 and of `hi` in bits 4-7.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo)
 {
