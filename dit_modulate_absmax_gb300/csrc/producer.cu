@@ -93,8 +93,17 @@ __device__ __forceinline__ int segment_of(const SegTable &t, int64_t r, int64_t 
 // Exact value of an E4M3 code with the sign bit clear (bias 7, 3 mantissa bits).
 __device__ __forceinline__ float e4m3_value(uint32_t c)
 {
-    const uint32_t e = (c >> 3) & 0xFu, mant = c & 7u;
-    return e ? __uint_as_float(((e + 120u) << 23) | (mant << 20)) : static_cast<float>(mant) * 0.001953125f;
+    // E4M3 -> f16 -> f32 with the hardware conversions: every E4M3 value
+    // (subnormals down to 2^-9 included) is exact in f16 and in f32.
+    float v;
+    asm("{\n\t.reg .b16 c2;\n\t.reg .b32 h2;\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.u16.u32 c2, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h2, c2;\n\t"
+        "mov.b32 {lo, hi}, h2;\n\t"
+        "cvt.f32.f16 %0, lo;\n\t}"
+        : "=f"(v)
+        : "r"(c & 0xFFu));
+    return v;
 }
 
 __device__ __forceinline__ float ex2_approx(float x)
