@@ -289,13 +289,15 @@ struct PlainSrc {  // already-materialised bf16 values (SwiGLU pass 2 with a wor
 // (above 0x7F80), which wins every later unsigned comparison.
 __device__ __forceinline__ uint32_t absmax16(const uint32_t (&y)[8])
 {
-    __nv_bfloat162 v = as_bf2(y[0] & 0x7FFF7FFFu);
+    // max.xorsign.abs: the magnitude of the result is max(|a|, |b|) (its sign
+    // is the xor of the inputs' signs, masked off at the end); .NaN makes a
+    // NaN input give a NaN.
+    uint32_t v = y[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i)
-        v = __hmax2_nan(v, as_bf2(y[i] & 0x7FFF7FFFu));
-    const uint32_t w = as_u32(v);
-    const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-    return max(lo, hi);   // both non-negative patterns: integer order = value order, NaN above all
+        asm("max.NaN.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(v) : "r"(y[i]));
+    v &= 0x7FFF7FFFu;
+    return max(v & 0xFFFFu, v >> 16);   // both non-negative patterns: integer order = value order, NaN above all
 }
 
 // ---------------------------------------------------------------------------
