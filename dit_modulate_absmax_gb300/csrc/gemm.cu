@@ -301,6 +301,65 @@ __device__ __forceinline__ bool store_rows_gated(const CUtensorMap *tmC, const C
     return true;
 }
 
+// store_rows_gated with the residual blocks prefetched through a ring of NB
+// 1 KB buffers (NB - 1 loads ahead), so that their load latency overlaps the
+// blocks being combined and stored instead of being paid once per block.
+// bars are NB mbarriers 8 bytes apart; bit b of `phases` is buffer b's phase.
+// A buffer is reloaded only after every earlier store of the warp has
+// finished reading shared memory (the last user of the buffer is the store of
+// the block NB - 1 places back).
+template <int NB>
+__device__ __forceinline__ bool store_rows_gated_ring(const CUtensorMap *tmC, const CUtensorMap *tmR, uint32_t buf,
+                                                      uint32_t bars, uint32_t &phases, const uint32_t (&pk)[64],
+                                                      int col0, int row0, int lane, const uint16_t *grow)
+{
+    constexpr int NC = 128 / CST_COLS;
+    if (lane == 0) {
+        bulk_wait_group_read0();   // the previous tile's stores have finished reading the buffers
+#pragma unroll
+        for (int c = 0; c < NB - 1; ++c) {
+            mbar_arrive_expect_tx(bars + 8 * c, CST_BYTES);
+            tma_load_2d(buf + c * CST_BYTES, tmR, col0 + c * CST_COLS, row0, bars + 8 * c);
+        }
+    }
+#pragma unroll   // constant indices into pk keep it in registers
+    for (int c = 0; c < NC; ++c) {
+        const int b = c % NB;
+        if (c + NB - 1 < NC && lane == 0) {
+            const int bp = (c + NB - 1) % NB;
+            bulk_wait_group_read0();   // block c - 1's store, the last reader of buffer bp, is done with it
+            mbar_arrive_expect_tx(bars + 8 * bp, CST_BYTES);
+            tma_load_2d(buf + bp * CST_BYTES, tmR, col0 + (c + NB - 1) * CST_COLS, row0, bars + 8 * bp);
+        }
+        __syncwarp();
+        if (!warp_wait(bars + 8 * b, (phases >> b) & 1u))
+            return false;
+        phases ^= 1u << b;
+        const uint32_t bb = buf + b * CST_BYTES;
+        const uint4 r0 = ld_shared_v4(bb + lane * 32);
+        const uint4 r1 = ld_shared_v4(bb + lane * 32 + 16);
+        const uint4 g0 = *reinterpret_cast<const uint4 *>(grow + col0 + c * CST_COLS);
+        const uint4 g1 = *reinterpret_cast<const uint4 *>(grow + col0 + c * CST_COLS + 8);
+        const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        uint32_t o[8];
+        const int w = c * (CST_COLS / 2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            o[i] = bf2_add_rn(rw[i], bf2_mul_rn(gw[i], pk[w + i]));
+        __syncwarp();   // every lane has read the residual before any lane overwrites the buffer
+        st_shared_v4(bb + lane * 32, o[0], o[1], o[2], o[3]);
+        st_shared_v4(bb + lane * 32 + 16, o[4], o[5], o[6], o[7]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, bb, col0 + c * CST_COLS, row0);
+            bulk_commit_group();
+        }
+    }
+    return true;
+}
+
 // Output tile t of the persistent schedule: groups of n_group N-tiles x all
 // M-tiles, N fastest inside a group (the last group may be narrower).
 __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int n_group, int &mt, int &nt)
@@ -869,6 +928,7 @@ constexpr int kFirstCopyWarp = 2;                   // leader: warps 2 and 3 cop
 constexpr int kCopyWarps = 2;
 constexpr int kFirstEpi = kFirstCopyWarp + kCopyWarps;   // epilogue warps 4 .. 11
 constexpr int kThreadsPair = 32 * (kFirstEpi + kEpiWarps);
+constexpr int kResBufs = 4;                         // gated epilogue: residual blocks in flight per warp
 
 // Stage geometry: BK = 256 K-elements per stage (128-byte operand rows with the
 // 128-byte swizzle), 5 stages.  (Stages of K = 128 -- 64-byte rows, 10 stages,
@@ -897,8 +957,8 @@ struct __align__(1024) Smem {
     uint8_t b[G::kStages][G::B_BYTES];
     uint8_t sfa[G::kStages][G::SFA_BYTES];
     uint8_t sfb[G::kStages][G::SFB_BYTES];
-    uint8_t cst[kEpiWarps][CST_BYTES];  // per epilogue warp: output staging for tensor stores
-    uint64_t res_full[kEpiWarps];       // per epilogue warp: a residual block landed in cst (gated epilogue)
+    uint8_t cst[kEpiWarps][kResBufs][CST_BYTES];   // per epilogue warp: staging for tensor loads and stores
+    uint64_t res_full[kEpiWarps][kResBufs];        // per epilogue warp and buffer: a residual block landed
     uint64_t full[G::kStages];          // leader: both CTAs' A and B landed and the copy warps' commits arrived
     uint64_t sf_full[G::kStages];       // leader: both CTAs' scale atoms landed
     uint64_t empty[G::kStages];         // both CTAs, arrived by the leader's commits
@@ -938,7 +998,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         mbar_init(smem_u32(&sm.acc_full), 1);
         mbar_init(smem_u32(&sm.acc_empty), 2 * kEpiWarps);
         for (int w = 0; w < kEpiWarps; ++w)
-            mbar_init(smem_u32(&sm.res_full[w]), 1);
+            for (int r = 0; r < kResBufs; ++r)
+                mbar_init(smem_u32(&sm.res_full[w][r]), 1);
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -1118,15 +1179,16 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 mbar_arrive_cluster_relaxed(leader_acc_empty);
             const int row0 = mt2 * 256 + static_cast<int>(rank) * pair::BM + q * 32;
             if (kGated) {
-                if (!store_rows_gated(&tmC, &tmR, smem_u32(sm.cst[warp - kFirstEpi]),
-                                      smem_u32(&sm.res_full[warp - kFirstEpi]), rphase, pk,
-                                      nt * pair::BN + half * 128, row0, lane, gate_row(ge, row0 + lane))) {
+                if (!store_rows_gated_ring<kResBufs>(&tmC, &tmR, smem_u32(sm.cst[warp - kFirstEpi][0]),
+                                                     smem_u32(&sm.res_full[warp - kFirstEpi][0]), rphase, pk,
+                                                     nt * pair::BN + half * 128, row0, lane,
+                                                     gate_row(ge, row0 + lane))) {
                     if (lane == 0)
                         record_error(ERR_WAIT_ACC);
                     break;
                 }
             } else {
-                store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpi]), pk, nt * pair::BN + half * 128, row0, lane);
+                store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpi][0]), pk, nt * pair::BN + half * 128, row0, lane);
             }
         }
         if (lane == 0)
