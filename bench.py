@@ -230,6 +230,8 @@ class Linear:
             events[0].record()
         if w.kind == "modulate":
             h3.modulate_absmax(a["x"], a["shift"], a["scale"], self.off, tensor_scale=self.ts, scratch=self.scratch)
+            if events is not None:
+                events[3].record()   # between pass 1 and pass 2
             h3.modulate_pack(a["x"], a["shift"], a["scale"], self.off, self.ts, w.m_pad, qdata=self.q, sfa=self.sfa)
         elif w.kind == "plain":
             h3.quantize_pack(a["x"], w.m_pad, tensor_scale=self.ts, scratch=self.scratch, qdata=self.q, sfa=self.sfa)
@@ -274,7 +276,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     assert h3.h3fp4_device_error() == 0
 
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in lins] for _ in range(args.steps)]
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in lins] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -294,11 +296,22 @@ def run_ours(args, rank, world, local_rank):
     elapsed_ms = max_over_ranks(start.elapsed_time(stop), dev)
     assert h3.h3fp4_device_error() == 0
 
+    def pct(xs, q):
+        xs = sorted(xs)
+        return xs[min(len(xs) - 1, int(round(q * (len(xs) - 1))))]
+
     per = {}
     for i, L in enumerate(lins):
         prod = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
         gem = [ev[k][i][1].elapsed_time(ev[k][i][2]) for k in range(args.steps)]
-        per[L.name] = {"producer_ms": sum(prod) / len(prod), "gemm_ms": sum(gem) / len(gem)}
+        per[L.name] = {"producer_ms": sum(prod) / len(prod), "gemm_ms": sum(gem) / len(gem),
+                       "producer_p50_p95": (pct(prod, 0.5), pct(prod, 0.95)),
+                       "gemm_p50_p95": (pct(gem, 0.5), pct(gem, 0.95))}
+        if L.w.kind == "modulate":   # the two producer passes separately
+            p1 = [ev[k][i][0].elapsed_time(ev[k][i][3]) for k in range(args.steps)]
+            p2 = [ev[k][i][3].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
+            per[L.name]["pass1_ms"] = sum(p1) / len(p1)
+            per[L.name]["pass2_ms"] = sum(p2) / len(p2)
 
     # end to end through the same C-ABI calls with host buffers
     host_in = [[x.cpu().pin_memory() for x in L.inputs()] for L in lins]
@@ -386,9 +399,14 @@ def run_ours(args, rank, world, local_rank):
         kernels[L.name] = {
             "producer_ms": round(p["producer_ms"], 4), "producer_gbs": round(gbs, 1),
             "producer_hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+            "producer_ms_p50_p95": [round(v, 4) for v in p["producer_p50_p95"]],
             "gemm_ms": round(p["gemm_ms"], 4), "gemm_tflops": round(tfl, 1),
+            "gemm_ms_p50_p95": [round(v, 4) for v in p["gemm_p50_p95"]],
             "epilogue": "gated residual" if L.gated else "bf16",
             "gemm_fp4_frac": round(tfl / fp4_peak, 4)}
+        if "pass1_ms" in p:
+            kernels[L.name]["pass1_ms"] = round(p["pass1_ms"], 4)
+            kernels[L.name]["pass2_ms"] = round(p["pass2_ms"], 4)
     dom = max(lins, key=lambda L: per[L.name]["gemm_ms"])
     dom_ms = per[dom.name]["gemm_ms"]
     achieved = dom.flops / (dom_ms * 1e-3) / 1e12
