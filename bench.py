@@ -209,7 +209,9 @@ class Linear:
         self.h = torch.empty(w.m, w.k, dtype=torch.int16, device=dev) if w.kind == "swiglu" else None
         self.flops = 2.0 * w.m * w.n * w.k
         self.prod_bytes = _bytes_per_element(w.kind) * w.m * w.k
-        self.launches = 3          # absmax kernel, pack kernel, GEMM kernel
+        # our kernels per run: modulation = absmax kernel + pack kernel + GEMM; the SwiGLU and
+        # plain producers run both passes in one cooperative launch (+ GEMM)
+        self.launches = 3 if w.kind == "modulate" else 2
         self.cfg = h3.GemmConfig(0, 0, gemm_kernel, 0) if gemm_kernel else None
         # gated residual epilogue: out = RN(res + RN(gate_s * C)), gate per stream segment
         self.gated = gated and name in GATED
