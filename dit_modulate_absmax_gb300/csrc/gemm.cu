@@ -6,39 +6,34 @@
 // NVFP4 Library Scheduling", Exact Operation: activation [M,K] times weight
 // [N,K], both K-major, row-major BF16 output, logical rows only).
 //
-// Persistent kernel, one CTA per SM, 10 warps:
-//   warp 0      TMA producer: per 256-wide K step, one 2-D tensor copy each for
-//               the A tile (128 rows x 128 bytes) and the B tile (256 x 128 bytes),
-//               both with 128-byte swizzle, plus 1-D bulk copies of the scale
-//               atoms (A: 4 atoms = 2 KB, B: 2 x 2 KB), into a 4-stage ring;
-//   warp 1      allocates TMEM, then one lane issues four
-//               tcgen05.mma kind::mxf4nvf4 (K = 64 each) per stage into the
-//               FP32 accumulator (TMEM columns 0-255); tcgen05.commit frees the
-//               stage and, after a tile's last stage, hands the accumulator to
-//               the epilogue;
-//   warps 10-13 scale warps, one per TMEM lane quarter: once a stage has
-//               landed they move its scale atoms from shared memory into TMEM
-//               with tcgen05.st (the MMA's scale layout) and arrive on the
-//               stage's sf_ready barrier, which the MMA lane waits on.  (Copying
-//               the atoms with tcgen05.cp instead costs twelve tensor-pipe
-//               instructions per stage, which measured as the main limiter.)
-//   warps 2-9   epilogue: each warp drains one 32-lane quarter x 128 columns of
-//               the accumulator into registers (tcgen05.ld), applying alpha and
-//               converting to bf16 as it goes, releases the accumulator at once
-//               so that the next tile's MMAs can start, and then writes its 32 x
-//               128 block with 16-column TMA tensor stores staged through a 1 KB
-//               shared-memory buffer of its own (per-lane stores from the
-//               row-per-lane accumulator layout would touch 32 rows per
-//               instruction; they measured 18% slower end to end).
-// Tiles (128 x 256 outputs) are visited in groups of n_group N-tiles x all
-// M-tiles with N fastest, so every 128-row A tile is used by n_group
-// consecutive tiles while it is L2-resident, and the B tiles of a group stay
-// resident while the group sweeps M (the N-group A-tile reuse factor).
-// The scales of stage s live in their own 48 TMEM columns (256 + 48 s), so a
-// later stage never overwrites scales an in-flight MMA still reads (the scale
-// warps refill stage s only after its loads, which follow the MMAs' commit).
-// Every pipeline wait gives up after 2 s and records a device error instead of
-// hanging.
+// Four kernels behind h3fp4_gemm (h3fp4_gemm_config.cta_pair), all
+// persistent, TMA-fed, with FP32 accumulators in TMEM and tcgen05.mma
+// kind::mxf4nvf4 block_scale scale_vec::4X (K = 64 per instruction):
+//   4 (default)  CTA pairs (cta_group::2) on 256 x 256 output tiles: per K step
+//                each CTA loads its 128 rows of A and of B and the step's scale
+//                atoms; in the leader, two copy warps copy the atoms into TMEM
+//                with tcgen05.cp and one MMA warp issues the four pair MMAs,
+//                every tcgen05 instruction issued warp-collectively through
+//                elect.sync (see the paircp namespace below);
+//   1            one CTA per 128 x 256 tile; four scale warps move the atoms
+//                into TMEM with tcgen05.st; one lane issues the MMAs;
+//   2            CTA pairs with scale warps handing their TMEM slots to the
+//                leader across the pair;
+//   3            clusters of two CTAs on the two 128-row halves of a 256 x 256
+//                block, the B tile and its scales multicast into both.
+// Shared by all: the epilogue warps drain 32 TMEM lanes x 128 columns each
+// (tcgen05.ld), apply alpha and round to bf16 as they go, release the
+// accumulator at once so that the next tile's MMAs can start, and write their
+// block with 16-column TMA tensor stores staged through shared memory (per-lane
+// stores from the row-per-lane accumulator layout touch 32 rows per
+// instruction and measured 18% slower end to end); optionally the gated
+// residual epilogue.  Tiles are visited in groups of n_group N-tiles x all
+// M-tiles with N fastest, so every A row block is used by n_group consecutive
+// tiles while it is L2-resident and a group's B tiles stay resident while it
+// sweeps M (the N-group A-tile reuse factor).  A stage's scales live in TMEM
+// columns of their own, rewritten only after the MMAs that read them have
+// committed.  Every pipeline wait gives up after 2 s and records a device
+// error instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
