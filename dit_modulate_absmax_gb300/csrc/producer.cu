@@ -46,7 +46,6 @@ constexpr int kBlock = 16;                          // values per thread and row
 constexpr int kRowsPerStep = 2 * kWarps;            // two rows per warp (one per half-warp)
 constexpr int kSteps = kTileRows / kRowsPerStep;    // 8
 constexpr int kUnroll = 2;                          // rows in flight per thread
-constexpr int kMinBlocks = 3;                       // resident CTAs per SM the register budget allows
 
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u)
 {
@@ -170,6 +169,7 @@ __device__ __forceinline__ void words(const Vec16 &v, uint32_t (&w)[8])
 }
 
 struct ModulateSrc {
+    static constexpr bool kModulated = true;
     const uint16_t *x;
     int64_t ldx;
     const uint16_t *shift;
@@ -213,6 +213,7 @@ struct ModulateSrc {
 };
 
 struct SwigluSrc {
+    static constexpr bool kModulated = false;
     const uint16_t *g;
     int64_t ldg;
     const uint16_t *u;
@@ -270,6 +271,7 @@ struct SwigluSrc {
 };
 
 struct PlainSrc {  // already-materialised bf16 values (SwiGLU pass 2 with a workspace)
+    static constexpr bool kModulated = false;
     const uint16_t *h;
     int64_t ldh;
 
@@ -283,6 +285,18 @@ struct PlainSrc {  // already-materialised bf16 values (SwiGLU pass 2 with a wor
     }
     __device__ __forceinline__ void keep(int64_t, int, const uint32_t (&)[8]) const {}
 };
+
+// Resident CTAs per SM that a kernel reading values from Src is compiled for
+// (the register budget): more warps hide more memory latency, until spills
+// cost more than that gains.  Measured at 37,810 rows: the modulation passes
+// 3 -> 4 per SM 6 % faster and 5 slower (the pack pass then spills ~200
+// bytes); the SwiGLU and plain single-launch producers 3 -> 4 -> 5 per SM
+// 0.806 -> 0.770 -> 0.747 ms and 0.251 -> 0.237 -> 0.232 ms.
+template <class Src>
+constexpr int min_blocks()
+{
+    return Src::kModulated ? 4 : 5;
+}
 
 // Bit pattern of max |y| over 16 bf16 values (two per word), with native
 // bf16x2 max on the absolute values; a NaN anywhere gives a NaN pattern
@@ -367,7 +381,7 @@ __device__ __forceinline__ float tensor_scale_of(uint32_t amax_bits)
 }
 
 template <class Src>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) absmax_kernel(Src src, int64_t m, int col_tiles, int64_t n_tiles,
+__global__ void __launch_bounds__(kThreads, min_blocks<Src>()) absmax_kernel(Src src, int64_t m, int col_tiles, int64_t n_tiles,
                                                           uint32_t *scratch, float *ts_out)
 {
     const uint32_t mx = cta_max(absmax_tiles(src, m, col_tiles, n_tiles));
@@ -553,7 +567,7 @@ __device__ __forceinline__ PackConsts pack_consts(float ts)
 // Pass 2: one CTA per 128 x 256 tile (tiles visited in reverse order).
 // ---------------------------------------------------------------------------
 template <class Src>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) pack_kernel(Src src, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
+__global__ void __launch_bounds__(kThreads, min_blocks<Src>()) pack_kernel(Src src, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
                                                         int64_t n_tiles, const float *ts_ptr, uint8_t *qdata,
                                                         uint8_t *sf)
 {
@@ -578,7 +592,7 @@ constexpr uint64_t kGridWaitLimitNs = 2000000000ull;
 constexpr uint32_t ERR_GRID_WAIT = 1u << 8;   // the cooperative producer's grid barrier timed out
 
 template <class Src1, class Src2>
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
+__global__ void __launch_bounds__(kThreads, min_blocks<Src1>())
     producer_coop_kernel(Src1 src1, Src2 src2, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
                          int64_t n_tiles1, int64_t n_tiles2, uint32_t *scratch, float *ts_out, uint8_t *qdata,
                          uint8_t *sf)
