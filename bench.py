@@ -130,8 +130,7 @@ class ClockSampler:
 # profile summary -> traffic of the dominant kernel (only while its source is unchanged)
 # ----------------------------------------------------------------------------
 # kernel behind each h3fp4_gemm_config.cta_pair value (0 = the library default)
-GEMM_KERNELS = {0: "nvf4_gemm_pair_cp_kernel", 1: "nvf4_gemm_kernel<single CTA>", 2: "nvf4_gemm_pair_kernel",
-                3: "nvf4_gemm_kernel<multicast pair>", 4: "nvf4_gemm_pair_cp_kernel"}
+GEMM_KERNELS = {0: "nvf4_gemm_pair_cp_kernel", 1: "nvf4_gemm_kernel<single CTA>", 4: "nvf4_gemm_pair_cp_kernel"}
 
 
 def _gemm_source_sha():
@@ -516,10 +515,9 @@ def main():
                     help="linear set: the benchmark's configs (default) or the model's own projection widths")
     ap.add_argument("--gated", action="store_true",
                     help="--widths h3: attention output and FC2 use the gated residual epilogue")
-    ap.add_argument("--gemm-kernel", type=int, default=0, choices=(0, 1, 2, 3, 4),
+    ap.add_argument("--gemm-kernel", type=int, default=0, choices=(0, 1, 4),
                     help="GEMM kernel (h3fp4_gemm_config.cta_pair): 0 library default (4), 1 single CTA, "
-                         "2 CTA pair with scale warps, 3 two-CTA cluster with B multicast, "
-                         "4 CTA pair with the scales copied into TMEM by a copy warp")
+                         "4 CTA pair with the scales copied into TMEM by copy warps")
     ap.add_argument("--profile-range", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()

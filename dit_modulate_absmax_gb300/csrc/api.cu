@@ -64,7 +64,7 @@ h3fp4_status check_pack_outputs(int64_t m, int64_t m_pad, const void *qdata, con
 {
     if (qdata == nullptr || sf == nullptr)
         return H3FP4_ERR_NULL;
-    if (m_pad < m || m_pad > INT32_MAX)
+    if (m_pad < m || m_pad % 16 != 0 || m_pad > INT32_MAX)   // the GEMM's descriptor M: a multiple of 16
         return H3FP4_ERR_SHAPE;
     if (!aligned16(qdata) || !aligned16(sf))
         return H3FP4_ERR_ALIGN;
@@ -186,7 +186,8 @@ h3fp4_status check_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a_
     *c = h3fp4_gemm_config{0, 0, 0, 0};
     if (cfg != nullptr) {
         *c = *cfg;
-        if (c->n_group < 0 || c->stages != 0 || c->cta_pair < 0 || c->cta_pair > 4 || c->reserved != 0)
+        if (c->n_group < 0 || c->stages != 0 || (c->cta_pair != 0 && c->cta_pair != 1 && c->cta_pair != 4) ||
+            c->reserved != 0)
             return H3FP4_ERR_UNSUPPORTED;
     }
     return H3FP4_OK;
@@ -235,8 +236,6 @@ h3fp4_status h3fp4_gemm_gated_residual(const uint8_t *a_q, const uint8_t *a_sf, 
         if (!same && o < r + rb && r < o + ob)
             return H3FP4_ERR_UNSUPPORTED;
     }
-    if (c.cta_pair == 2)
-        return H3FP4_ERR_UNSUPPORTED;
     h3fp4::GatedArgs g{static_cast<const uint16_t *>(gate_bf16), ld_gate, seg, residual_bf16, ldr};
     return h3fp4::launch_gemm(a_q, a_sf, a_tensor_scale, b_q, b_sf, b_tensor_scale, static_cast<uint16_t *>(out_bf16),
                               ldo, m, m_pad, n, k, c, &g, as_stream(stream));

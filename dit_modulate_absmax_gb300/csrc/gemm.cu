@@ -6,22 +6,21 @@
 // NVFP4 Library Scheduling", Exact Operation: activation [M,K] times weight
 // [N,K], both K-major, row-major BF16 output, logical rows only).
 //
-// Four kernels behind h3fp4_gemm (h3fp4_gemm_config.cta_pair), all
+// Two kernels behind h3fp4_gemm (h3fp4_gemm_config.cta_pair), both
 // persistent, TMA-fed, with FP32 accumulators in TMEM and tcgen05.mma
-// kind::mxf4nvf4 block_scale scale_vec::4X (K = 64 per instruction):
-//   4 (default)  CTA pairs (cta_group::2) on 256 x 256 output tiles: per K step
-//                each CTA loads its 128 rows of A and of B and the step's scale
-//                atoms; in the leader, two copy warps copy the atoms into TMEM
-//                with tcgen05.cp and one MMA warp issues the four pair MMAs,
-//                every tcgen05 instruction issued warp-collectively through
-//                elect.sync (see the paircp namespace below);
+// kind::mxf4nvf4 block_scale scale_vec::4X, each 256-element K stage covered
+// by two K = 96 instructions and one K = 64 (see kStageMmas):
+//   0 / 4 (default)  CTA pairs (cta_group::2) on 256 x 256 output tiles: per K
+//                step each CTA loads its 128 rows of A and of B and the step's
+//                scale atoms; in the leader, two copy warps copy the atoms into
+//                TMEM with tcgen05.cp and one MMA warp issues the three pair
+//                MMAs, every tcgen05 instruction issued warp-collectively
+//                through elect.sync (see the paircp namespace below);
 //   1            one CTA per 128 x 256 tile; four scale warps move the atoms
-//                into TMEM with tcgen05.st; one lane issues the MMAs;
-//   2            CTA pairs with scale warps handing their TMEM slots to the
-//                leader across the pair;
-//   3            clusters of two CTAs on the two 128-row halves of a 256 x 256
-//                block, the B tile and its scales multicast into both.
-// Shared by all: the epilogue warps drain 32 TMEM lanes x 128 columns each
+//                into TMEM with tcgen05.st; one lane issues the MMAs.
+// Every operand load is a plain (non-multicast) TMA copy into the issuing
+// CTA's own shared memory.
+// Shared by both: the epilogue warps drain 32 TMEM lanes x 128 columns each
 // (tcgen05.ld), apply alpha and round to bf16 as they go, release the
 // accumulator at once so that the next tile's MMAs can start, and write their
 // block with 16-column TMA tensor stores staged through shared memory (per-lane
@@ -107,6 +106,30 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n)
 {
     return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
+
+// The block-scaled MMAs of one 256-element K stage.  On sm_103a the
+// instruction descriptor's bit 31 selects a dense K of 96 instead of 64 for
+// the E2M1 kinds: 1.5x the work per instruction in about the same tensor-pipe
+// time (a one-CTA microbenchmark: 43.6k against 28.2k FLOP per SM clock).
+// One instruction may not cross the 128-byte swizzled row that holds a
+// stage's 256 elements of an operand row, so a stage takes K = 96 at elements
+// 0 and 96 and K = 64 at element 192: three instructions instead of four.  The
+// scale-factor id (descriptor bits 29-30 for A, 4-5 for B) is the byte of the
+// 32-bit TMEM scale word at which the instruction's first scale sits: the
+// second K = 96 MMA starts at scale block 6, byte 2 of the word that holds
+// blocks 4-7, and reads on into the next word.
+constexpr int kStageMmas = 3;
+__host__ __device__ constexpr uint32_t stage_mma_k0(int j) { return j == 0 ? 0u : (j == 1 ? 96u : 192u); }
+// descriptor start-address advance, in 16-byte units (two E2M1 values per byte)
+__host__ __device__ constexpr uint32_t stage_mma_desc(int j) { return stage_mma_k0(j) / 32; }
+// the group of 4 scale blocks (one 128x4 atom, one TMEM column per 32 rows) holding the first scale
+__host__ __device__ constexpr uint32_t stage_mma_chunk(int j) { return stage_mma_k0(j) / 64; }
+__host__ __device__ constexpr uint32_t stage_mma_idesc(uint32_t base, int j)
+{
+    return j < 2 ? base | (1u << 31) | (((stage_mma_k0(j) / 16) % 4) << 29) | (((stage_mma_k0(j) / 16) % 4) << 4)
+                 : base;
+}
+static_assert(stage_mma_k0(1) + 96 <= stage_mma_k0(2) && stage_mma_k0(2) + 64 == 256, "a stage covers K = 256");
 
 __device__ __forceinline__ void record_error(uint32_t code) { atomicOr(&g_device_error, code); }
 
@@ -367,19 +390,11 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
     mt = tt / ng;
 }
 
-// kMcast = false: one CTA per output tile.  kMcast = true: clusters of two
-// CTAs take the two M tiles (2 mt2, 2 mt2 + 1) of one N tile together.  Each
-// CTA still loads its own A tile and A scales and runs its own MMAs, scale
-// staging and epilogue, but loads only its 128-row half of the B tile and of
-// the B scales, multicast into both CTAs: the tensor-copy bytes an SM issues
-// per K step drop from 54 KB to 36 KB.  A stage is refilled once the MMAs of
-// both CTAs have read it (the MMA commits arrive on both CTAs' empty
-// barriers), and the CTAs leave together (a cluster barrier) so that no
-// multicast copy or commit targets a CTA that has exited.  Rank 1 of the last
-// cluster may hold an M tile past the last one when the M tile count is odd:
-// its A rows read as zero, its A scales are not loaded and its output rows are
-// clipped by the tensor stores.
-template <bool kMcast, bool kGated>
+// One CTA per 128 x 256 output tile: warp 0 loads A, B and their scale atoms
+// into a 4-stage ring, four scale warps move each stage's atoms into TMEM with
+// tcgen05.st, one lane of warp 1 issues the MMAs, eight warps drain the
+// accumulator.
+template <bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
@@ -393,23 +408,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kt_count = k / BK;
     const int64_t atoms_per_rb = k / 64;           // scale atoms per 128-row block
     const int n_rb = (n + 127) / 128;
-    const int rank = kMcast ? static_cast<int>(cluster_ctarank()) : 0;
-    const int sched_first = kMcast ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int sched_step = kMcast ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-    const int m_sched = kMcast ? (m_tiles + 1) >> 1 : m_tiles;     // M positions of the schedule
-    const int total_tiles = m_sched * n_tiles;
-    // this CTA's output tile for schedule position t
-    auto coords = [&](int t, int &mt, int &nt) {
-        int ms;
-        tile_coords(t, m_sched, n_tiles, n_group, ms, nt);
-        mt = kMcast ? 2 * ms + rank : ms;
-    };
+    const int sched_first = static_cast<int>(blockIdx.x);
+    const int sched_step = static_cast<int>(gridDim.x);
+    const int total_tiles = m_tiles * n_tiles;
+    auto coords = [&](int t, int &mt, int &nt) { tile_coords(t, m_tiles, n_tiles, n_group, mt, nt); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.sf_full[s]), 1);
-            mbar_init(smem_u32(&sm.empty[s]), kMcast ? 2 : 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
             mbar_init(smem_u32(&sm.sf_ready[s]), kScaleWarps);
         }
         mbar_init(smem_u32(&sm.acc_full), 1);
@@ -428,10 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    if (kMcast)
-        cluster_sync();   // the peer's barriers are initialised before any multicast reaches them
-    else
-        __syncthreads();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
@@ -442,9 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = sched_first; t < total_tiles && ok; t += sched_step) {
                 int mt, nt;
                 coords(t, mt, nt);
-                const bool has_a = mt < m_tiles;            // (only false for rank 1 of the last cluster)
                 const bool has_rb1 = (2 * nt + 1) < n_rb;   // second 128-row half of the B tile exists
-                const uint32_t sf_tx = (has_a ? SFA_BYTES : 0u) + (has_rb1 ? SFB_BYTES : SFB_BYTES / 2);
+                const uint32_t sf_tx = SFA_BYTES + (has_rb1 ? SFB_BYTES : SFB_BYTES / 2);
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
@@ -456,29 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // scales first (small; the scale warps stage them while A and B are in flight)
                     const uint32_t sbar = smem_u32(&sm.sf_full[s]);
                     mbar_arrive_expect_tx(sbar, sf_tx);
-                    if (has_a)
-                        bulk_load(smem_u32(sm.sfa[s]), a_sf + (mt * atoms_per_rb + kt * 4) * ATOM, SFA_BYTES, sbar);
-                    if (kMcast) {
-                        // this CTA's half of the B scales, into both CTAs
-                        if (2 * nt + rank < n_rb)
-                            bulk_load_mcast(smem_u32(sm.sfb[s]) + rank * (SFB_BYTES / 2),
-                                            b_sf + ((2 * nt + rank) * atoms_per_rb + kt * 4) * ATOM, SFB_BYTES / 2,
-                                            sbar, 0x3);
-                    } else {
-                        bulk_load(smem_u32(sm.sfb[s]), b_sf + ((2 * nt) * atoms_per_rb + kt * 4) * ATOM,
-                                  SFB_BYTES / 2, sbar);
-                        if (has_rb1)
-                            bulk_load(smem_u32(sm.sfb[s]) + SFB_BYTES / 2,
-                                      b_sf + ((2 * nt + 1) * atoms_per_rb + kt * 4) * ATOM, SFB_BYTES / 2, sbar);
-                    }
+                    bulk_load(smem_u32(sm.sfa[s]), a_sf + (mt * atoms_per_rb + kt * 4) * ATOM, SFA_BYTES, sbar);
+                    bulk_load(smem_u32(sm.sfb[s]), b_sf + ((2 * nt) * atoms_per_rb + kt * 4) * ATOM, SFB_BYTES / 2,
+                              sbar);
+                    if (has_rb1)
+                        bulk_load(smem_u32(sm.sfb[s]) + SFB_BYTES / 2,
+                                  b_sf + ((2 * nt + 1) * atoms_per_rb + kt * 4) * ATOM, SFB_BYTES / 2, sbar);
                     const uint32_t bar = smem_u32(&sm.full[s]);
                     mbar_arrive_expect_tx(bar, A_BYTES + B_BYTES);
                     tma_load_2d(smem_u32(sm.a[s]), &tmA, kt * BKB, mt * BM, bar);
-                    if (kMcast)   // this CTA's 128-row half of the B tile, into both CTAs
-                        tma_load_2d_mcast(smem_u32(sm.b[s]) + rank * (B_BYTES / 2), &tmB, kt * BKB,
-                                          nt * BN + rank * (BN / 2), bar, 0x3);
-                    else
-                        tma_load_2d(smem_u32(sm.b[s]), &tmB, kt * BKB, nt * BN, bar);
+                    tma_load_2d(smem_u32(sm.b[s]), &tmB, kt * BKB, nt * BN, bar);
                 }
             }
         }
@@ -510,15 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, 1024, 2);
                     const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, 1024, 2);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        // K step j: 64 elements = 32 bytes further along the swizzled row.
-                        tc_mma_nvf4(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, idesc, sfa_t + 4 * j,
-                                    sfb_t + 8 * j, (kt | j) != 0);
-                    }
-                    if (kMcast)
-                        tc_commit_mc(smem_u32(&sm.empty[s]), 0x3);   // the stage is free in both CTAs' eyes
-                    else
-                        tc_commit(smem_u32(&sm.empty[s]));
+                    for (int j = 0; j < kStageMmas; ++j)
+                        tc_mma_nvf4(tmem + ACC_COL, a_desc + stage_mma_desc(j), b_desc + stage_mma_desc(j),
+                                    stage_mma_idesc(idesc, j), sfa_t + 4 * stage_mma_chunk(j),
+                                    sfb_t + 8 * stage_mma_chunk(j), (kt | j) != 0);
+                    tc_commit(smem_u32(&sm.empty[s]));
                 }
                 if (ok)
                     tc_commit(smem_u32(&sm.acc_full));
@@ -607,291 +594,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     tc_fence_before();
-    if (kMcast)
-        cluster_sync();   // no CTA leaves while its peer may still multicast into it or commit to it
-    else
-        __syncthreads();
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
 }
-
-// ---------------------------------------------------------------------------
-// CTA-pair variant (tcgen05 cta_group::2).  A cluster of two CTAs on two SMs
-// computes a 256 x 256 output tile: each CTA loads its own 128 rows of A and
-// its own 128 rows (output columns) of B per K step, plus its 128 rows of A
-// scales and all 256 rows of B scales; the leader CTA (rank 0) issues the pair
-// MMA (M = 256) whose accumulator rows 0-127 land in the leader's TMEM and
-// rows 128-255 in the peer's.  (Each CTA's rows read their A scales and all
-// 256 columns' B scales from that CTA's own TMEM, so both CTAs stage the full
-// B scales.)  Per SM and K step this moves 38 KB instead of 54 KB for the same
-// MMA work.  The 32 KB of A and B sit in a 6-stage ring; the 6 KB of scales
-// in a 4-slot shared-memory ring of their own and then in 5 TMEM slots.
-//   - Both CTAs' A and B loads complete on the leader's full barrier (the
-//     peer's through the cta_group::2 form of the tensor copy).  Each CTA's
-//     scale atoms complete on its own sf_full barrier; its scale warps read
-//     them into registers (freeing the slot through sf_empty), wait until the
-//     MMAs that last used their TMEM slot completed (sf_free), stage them and
-//     arrive on the leader's sf_ready barrier (8 arrivals: 4 warps x 2 CTAs,
-//     relaxed: a cluster-scope release measured at 1,500 cycles per arrive).
-//     The MMA thread waits on full and sf_ready.
-//   - The leader's commits arrive on the barriers of both CTAs (multicast):
-//     an A/B stage and a TMEM scale slot are free in both CTAs once the pair's
-//     MMAs have read them.
-//   - Each CTA's epilogue drains its own accumulator rows, arrives on the
-//     leader's accumulator-empty barrier (16 arrivals: 8 warps x 2 CTAs) and
-//     writes its rows with tensor stores as in the single-CTA kernel.
-// ---------------------------------------------------------------------------
-namespace pair {
-
-constexpr int BM = 128;                    // rows per CTA; the pair covers 256
-constexpr int BN = 256;                    // output columns per pair tile
-constexpr int kStages = 6;                 // A/B ring
-constexpr int kSfSlots = 4;                // shared-memory scale ring
-constexpr int kTmemSlots = 5;              // TMEM scale slots (48 columns each, from column 256)
-constexpr uint32_t A_BYTES = BM * BKB;     // 16 KB
-constexpr uint32_t B_BYTES = 128 * BKB;    // 16 KB: this CTA's half of the B tile
-constexpr uint32_t SFA_BYTES = 4 * ATOM;   // this CTA's 128 rows x 16 scales
-constexpr uint32_t SFB_BYTES = 8 * ATOM;   // all 256 B rows x 16 scales
-constexpr uint32_t SF_ROW = 256;           // row length of the scale tensor maps
-
-struct __align__(1024) Smem {
-    uint8_t a[kStages][A_BYTES];
-    uint8_t b[kStages][B_BYTES];
-    uint8_t sfa[kSfSlots][SFA_BYTES];
-    uint8_t sfb[kSfSlots][SFB_BYTES];
-    uint8_t cst[kEpiWarps][CST_BYTES];  // per epilogue warp: output staging for tensor stores
-    uint64_t full[kStages];          // leader: both CTAs' A and B tiles landed
-    uint64_t empty[kStages];         // both CTAs, arrived by the leader's commits
-    uint64_t sf_full[kSfSlots];      // this CTA's scale atoms landed
-    uint64_t sf_empty[kSfSlots];     // this CTA's scale warps have read a slot
-    uint64_t sf_ready[kTmemSlots];   // leader: both CTAs' scales staged in a TMEM slot
-    uint64_t sf_free[kTmemSlots];    // both CTAs: the MMAs reading a TMEM slot completed
-    uint64_t acc_full;               // both CTAs
-    uint64_t acc_empty;          // used in the leader
-    uint32_t tmem_base;
-};
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
-
-__global__ void __launch_bounds__(kThreads, 1)
-    nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                          const __grid_constant__ CUtensorMap tmC, const float *__restrict__ a_ts,
-                          const float *__restrict__ b_ts, int m, int n, int k, int m_tiles2, int n_tiles, int n_group,
-                          int sfa_rbs, int sfb_rbs)
-{
-    extern __shared__ uint8_t smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
-    const int kt_count = k / BK;
-    const int chunks_per_rb = k / 256;          // 2 KB scale chunks per 128-row block
-    const int total_tiles = m_tiles2 * n_tiles;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&sm.full[s]), 1);
-            mbar_init(smem_u32(&sm.empty[s]), 1);
-        }
-        for (int s = 0; s < kSfSlots; ++s) {
-            mbar_init(smem_u32(&sm.sf_full[s]), 1);
-            mbar_init(smem_u32(&sm.sf_empty[s]), kScaleWarps);
-        }
-        for (int s = 0; s < kTmemSlots; ++s) {
-            mbar_init(smem_u32(&sm.sf_ready[s]), 2 * kScaleWarps);
-            mbar_init(smem_u32(&sm.sf_free[s]), 1);
-        }
-        mbar_init(smem_u32(&sm.acc_full), 1);
-        mbar_init(smem_u32(&sm.acc_empty), 2 * kEpiWarps);
-        fence_mbar_init();
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
-        prefetch_tmap(&tmSFA);
-        prefetch_tmap(&tmSFB);
-        prefetch_tmap(&tmC);
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(smem_u32(&sm.tmem_base), TMEM_COLS);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before();
-    cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
-    tc_fence_after();
-    const uint32_t tmem = sm.tmem_base;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (int t = pair_id; t < total_tiles && ok; t += num_pairs) {
-                int mt2, nt;
-                tile_coords(t, m_tiles2, n_tiles, n_group, mt2, nt);
-                const int rb_a = 2 * mt2 + static_cast<int>(rank);
-                const bool has_sfa = rb_a < sfa_rbs;   // else every row of this half is padding
-                const bool has_b1 = 2 * nt + 1 < sfb_rbs;
-                const uint32_t sf_tx = (has_sfa ? SFA_BYTES : 0u) + (has_b1 ? SFB_BYTES : SFB_BYTES / 2);
-                for (int kt = 0; kt < kt_count; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1;
-                    const int f = it % kSfSlots;
-                    if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ph ^ 1u, kWaitLimitNs) ||
-                        !mbar_wait_bounded(smem_u32(&sm.sf_empty[f]), ((it / kSfSlots) & 1) ^ 1u, kWaitLimitNs)) {
-                        record_error(ERR_WAIT_EMPTY);
-                        ok = false;
-                        break;
-                    }
-                    // scales first, on this CTA's own barrier (its scale warps stage them)
-                    const uint32_t sbar = smem_u32(&sm.sf_full[f]);
-                    mbar_arrive_expect_tx(sbar, sf_tx);
-                    if (has_sfa)
-                        tma_load_2d(smem_u32(sm.sfa[f]), &tmSFA, 0, (rb_a * chunks_per_rb + kt) * 8, sbar);
-                    tma_load_2d(smem_u32(sm.sfb[f]), &tmSFB, 0, (2 * nt * chunks_per_rb + kt) * 8, sbar);
-                    if (has_b1)
-                        tma_load_2d(smem_u32(sm.sfb[f]) + SFB_BYTES / 2, &tmSFB, 0,
-                                    ((2 * nt + 1) * chunks_per_rb + kt) * 8, sbar);
-                    // A and B halves of both CTAs complete on the leader's full barrier
-                    if (rank == 0)
-                        mbar_arrive_expect_tx(smem_u32(&sm.full[s]), 2 * (A_BYTES + B_BYTES));
-                    const uint32_t bar = mapa_shared(smem_u32(&sm.full[s]), 0);
-                    tma_load_2d_pair(smem_u32(sm.a[s]), &tmA, kt * BKB, mt2 * 256 + static_cast<int>(rank) * 128, bar);
-                    tma_load_2d_pair(smem_u32(sm.b[s]), &tmB, kt * BKB, nt * BN + static_cast<int>(rank) * 128, bar);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc = idesc_nvf4(2 * BM, BN);
-            uint32_t it = 0, local = 0;
-            bool ok = true;
-            for (int t = pair_id; t < total_tiles && ok; t += num_pairs, ++local) {
-                if (!mbar_wait_bounded(smem_u32(&sm.acc_empty), (local & 1) ^ 1u, kWaitLimitNs)) {
-                    record_error(ERR_WAIT_ACC_EMPTY);
-                    break;
-                }
-                tc_fence_after();
-                for (int kt = 0; kt < kt_count; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1;
-                    const int ts = it % kTmemSlots;
-                    // both CTAs' A and B landed and both CTAs' scales are in TMEM
-                    if (!mbar_wait_bounded(smem_u32(&sm.full[s]), ph, kWaitLimitNs) ||
-                        !mbar_wait_bounded(smem_u32(&sm.sf_ready[ts]), (it / kTmemSlots) & 1, kWaitLimitNs)) {
-                        record_error(ERR_WAIT_FULL);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sfa_t = tmem + SF_COL + ts * SF_COLS_PER_STAGE;
-                    const uint32_t sfb_t = sfa_t + 16;
-                    const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, 1024, 2);
-                    const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, 1024, 2);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        tc_mma_nvf4_pair(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, idesc, sfa_t + 4 * j,
-                                         sfb_t + 8 * j, (kt | j) != 0);
-                    tc_commit_pair_mc(smem_u32(&sm.empty[s]), 0x3);
-                    tc_commit_pair_mc(smem_u32(&sm.sf_free[ts]), 0x3);
-                }
-                if (ok)
-                    tc_commit_pair_mc(smem_u32(&sm.acc_full), 0x3);
-            }
-        }
-    } else if (warp >= kFirstScaleWarp) {
-        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t leader_sf_ready = mapa_shared(smem_u32(&sm.sf_ready[0]), 0);
-        uint32_t it = 0;
-        bool ok = true;
-        for (int t = pair_id; t < total_tiles && ok; t += num_pairs) {
-            for (int kt = 0; kt < kt_count; ++kt, ++it) {
-                const int f = it % kSfSlots;
-                const int ts = it % kTmemSlots;
-                if (!warp_wait(smem_u32(&sm.sf_full[f]), (it / kSfSlots) & 1)) {
-                    if (lane == 0)
-                        record_error(ERR_WAIT_SCALES);
-                    ok = false;
-                    break;
-                }
-                uint32_t a[16], b[32];
-                read_scales(sm.sfa[f], sm.sfb[f], lane, a, b);
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&sm.sf_empty[f]));   // the values are in registers
-                // the pair's MMAs that last read this TMEM slot have completed
-                if (!warp_wait(smem_u32(&sm.sf_free[ts]), ((it / kTmemSlots) & 1) ^ 1u)) {
-                    if (lane == 0)
-                        record_error(ERR_WAIT_SCALES);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_st_32x32b_x16(tmem + lane_base + SF_COL + ts * SF_COLS_PER_STAGE, a);
-                tmem_st_32x32b_x32(tmem + lane_base + SF_COL + ts * SF_COLS_PER_STAGE + 16, b);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)   // relaxed: only tcgen05 stores are handed off, ordered by the fences
-                    mbar_arrive_cluster_relaxed(leader_sf_ready + ts * 8);
-            }
-        }
-    } else {
-        const int q = warp & 3;
-        const int half = (warp - kFirstEpiWarp) >> 2;
-        const float alpha = __fmul_rn(*a_ts, *b_ts);
-        const uint32_t leader_acc_empty = mapa_shared(smem_u32(&sm.acc_empty), 0);
-        uint32_t local = 0;
-        for (int t = pair_id; t < total_tiles; t += num_pairs, ++local) {
-            int mt2, nt;
-            tile_coords(t, m_tiles2, n_tiles, n_group, mt2, nt);
-            bool ok = false;
-            if (lane == 0)
-                ok = mbar_wait_bounded(smem_u32(&sm.acc_full), local & 1, kWaitLimitNs);
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            __syncwarp();
-            if (!ok) {
-                if (lane == 0)
-                    record_error(ERR_WAIT_ACC);
-                break;
-            }
-            tc_fence_after();
-            // Drain 32 columns at a time, applying alpha and rounding to bf16 at
-            // once, so that only the packed half-width results stay live.
-            uint32_t pk[64];
-            const uint32_t base = tmem + (static_cast<uint32_t>(q * 32) << 16) + ACC_COL + half * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(base + 32 * c, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float lo = __fmul_rn(alpha, __uint_as_float(v[2 * i]));
-                    const float hi = __fmul_rn(alpha, __uint_as_float(v[2 * i + 1]));
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-                    memcpy(&pk[16 * c + i], &b2, 4);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)   // this CTA's rows are drained (relaxed: earlier tiles' stores need not land first)
-                mbar_arrive_cluster_relaxed(leader_acc_empty);
-            store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpiWarp]), pk, nt * BN + half * 128,
-                       mt2 * 256 + static_cast<int>(rank) * BM + q * 32, lane);
-        }
-        if (lane == 0)
-            bulk_wait_group0();
-    }
-
-    tc_fence_before();
-    cluster_sync();   // no CTA leaves while its peer may still touch its barriers or TMEM
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc_pair(tmem, TMEM_COLS);
-    }
-}
-
-}  // namespace pair
 
 // ---------------------------------------------------------------------------
 // CTA-pair kernel with the scales copied into TMEM by tcgen05.cp
@@ -919,6 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 namespace paircp {
 
+constexpr int PBM = 128;                         // rows per CTA; the pair covers 256
+constexpr int PBN = 256;                         // output columns per pair tile
+constexpr uint32_t SF_ROW = 256;                 // row length of the scale tensor maps
 constexpr int kFirstCopyWarp = 2;                   // leader: warps 2 and 3 copy the scale atoms into TMEM
 constexpr int kCopyWarps = 2;
 constexpr int kFirstEpi = kFirstCopyWarp + kCopyWarps;   // epilogue warps 4 .. 11
@@ -932,15 +643,15 @@ constexpr int kResBufs = 4;                         // gated epilogue: residual 
 // waits on.)
 struct Geo {
     static constexpr int kStages = 5;
-    static constexpr int kMmas = BK / 64;                   // K = 64 per MMA
+    static constexpr int kChunks = BK / 64;                 // scale atoms (4 scale blocks each) per 128 rows
     static constexpr uint32_t ROW = BKB;                    // bytes of one operand row per stage
     static constexpr uint32_t A_BYTES = 128 * ROW;          // this CTA's 128 rows of A
     static constexpr uint32_t B_BYTES = 128 * ROW;          // this CTA's 128 rows of B
-    static constexpr uint32_t SFA_BYTES = kMmas * ATOM;     // this CTA's A scale atoms
-    static constexpr uint32_t SFB_BYTES = 2 * kMmas * ATOM; // all 256 B rows' scale atoms
+    static constexpr uint32_t SFA_BYTES = kChunks * ATOM;     // this CTA's A scale atoms
+    static constexpr uint32_t SFB_BYTES = 2 * kChunks * ATOM; // all 256 B rows' scale atoms
     static constexpr uint32_t AB_TX = 2 * (A_BYTES + B_BYTES);        // both CTAs' operands of a stage
     static constexpr uint32_t SF_TX = 2 * (SFA_BYTES + SFB_BYTES);    // both CTAs' scale atoms of a stage
-    static constexpr uint32_t SF_COLS = 12 * kMmas;         // TMEM columns of one stage's scales
+    static constexpr uint32_t SF_COLS = 12 * kChunks;       // TMEM columns of one stage's scales
     static constexpr uint32_t LAYOUT = 2;                   // descriptor swizzle mode: 128 B
     static constexpr uint32_t SBO = 8 * ROW;                // bytes between 8-row core-matrix groups
     static_assert(SF_COL + kStages * SF_COLS <= TMEM_COLS, "TMEM scale slots");
@@ -1043,7 +754,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                     const uint32_t bar = mapa_shared(smem_u32(&sm.full[s]), 0);
                     tma_load_2d_pair(smem_u32(sm.a[s]), &tmA, kt * G::ROW, mt2 * 256 + static_cast<int>(rank) * 128,
                                      bar);
-                    tma_load_2d_pair(smem_u32(sm.b[s]), &tmB, kt * G::ROW, nt * pair::BN + static_cast<int>(rank) * 128,
+                    tma_load_2d_pair(smem_u32(sm.b[s]), &tmB, kt * G::ROW, nt * PBN + static_cast<int>(rank) * 128,
                                      bar);
                 }
             }
@@ -1055,7 +766,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         // warps split the stage's MMAs between them (6 copies each).  A slot is
         // rewritten only after its stage's scale barrier completed again, i.e.
         // after the producers saw the commit of the MMAs that last read it.
-        constexpr int kPerWarp = G::kMmas / kCopyWarps;
+        constexpr int kPerWarp = G::kChunks / kCopyWarps;
         const int j0 = (warp - kFirstCopyWarp) * kPerWarp;
         if (rank == 0) {
             uint32_t it = 0;
@@ -1071,7 +782,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                     }
                     tc_fence_after();
                     const uint32_t sfa_t = tmem + SF_COL + s * G::SF_COLS;
-                    const uint32_t sfb_t = sfa_t + 4 * G::kMmas;
+                    const uint32_t sfb_t = sfa_t + 4 * G::kChunks;
                     const uint32_t sfa_s = smem_u32(sm.sfa[s]), sfb_s = smem_u32(sm.sfb[s]);
 #pragma unroll
                     for (int j = j0; j < j0 + kPerWarp; ++j) {
@@ -1092,7 +803,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         // per-stage issue time, which the tensor pipe otherwise waits on,
         // drops well below the MMAs' own time.
         if (rank == 0) {
-            constexpr uint32_t idesc = idesc_nvf4(2 * pair::BM, pair::BN);
+            constexpr uint32_t idesc = idesc_nvf4(2 * PBM, PBN);
             const int my_tiles = pair_id < total_tiles ? (total_tiles - pair_id + num_pairs - 1) / num_pairs : 0;
             const uint32_t total_steps = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(kt_count);
             uint32_t it = 0, local = 0;
@@ -1115,13 +826,14 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                     }
                     tc_fence_after();
                     const uint32_t sfa_t = tmem + SF_COL + s * G::SF_COLS;
-                    const uint32_t sfb_t = sfa_t + 4 * G::kMmas;
+                    const uint32_t sfb_t = sfa_t + 4 * G::kChunks;
                     const uint64_t a_desc = smem_desc(smem_u32(sm.a[s]), 0, G::SBO, G::LAYOUT);
                     const uint64_t b_desc = smem_desc(smem_u32(sm.b[s]), 0, G::SBO, G::LAYOUT);
 #pragma unroll
-                    for (int j = 0; j < G::kMmas - 1; ++j)
-                        tc_mma_nvf4_pair_elect(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, idesc, sfa_t + 4 * j,
-                                               sfb_t + 8 * j, (kt | j) != 0);
+                    for (int j = 0; j < kStageMmas - 1; ++j)
+                        tc_mma_nvf4_pair_elect(tmem + ACC_COL, a_desc + stage_mma_desc(j), b_desc + stage_mma_desc(j),
+                                               stage_mma_idesc(idesc, j), sfa_t + 4 * stage_mma_chunk(j),
+                                               sfb_t + 8 * stage_mma_chunk(j), (kt | j) != 0);
                     // While this stage's MMAs run, look (without waiting) whether the next
                     // stage is already complete; if so the next iteration skips its wait,
                     // whose latency otherwise lands between two stages' MMAs.
@@ -1129,9 +841,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                     known_ready = nx < total_steps &&
                                   __all_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&sm.full[nx % kStages]),
                                                                          (nx / kStages) & 1));
-                    constexpr int jl = G::kMmas - 1;
-                    tc_mma_nvf4_pair_elect(tmem + ACC_COL, a_desc + 2 * jl, b_desc + 2 * jl, idesc, sfa_t + 4 * jl,
-                                           sfb_t + 8 * jl, 1u);
+                    constexpr int jl = kStageMmas - 1;
+                    tc_mma_nvf4_pair_elect(tmem + ACC_COL, a_desc + stage_mma_desc(jl), b_desc + stage_mma_desc(jl),
+                                           stage_mma_idesc(idesc, jl), sfa_t + 4 * stage_mma_chunk(jl),
+                                           sfb_t + 8 * stage_mma_chunk(jl), 1u);
                     tc_commit_pair_mc_elect(smem_u32(&sm.empty[s]), 0x3);
                 }
                 if (ok)
@@ -1172,18 +885,18 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             __syncwarp();
             if (lane == 0)   // this CTA's rows are drained (relaxed: earlier tiles' stores need not land first)
                 mbar_arrive_cluster_relaxed(leader_acc_empty);
-            const int row0 = mt2 * 256 + static_cast<int>(rank) * pair::BM + q * 32;
+            const int row0 = mt2 * 256 + static_cast<int>(rank) * PBM + q * 32;
             if (kGated) {
                 if (!store_rows_gated_ring<kResBufs>(&tmC, &tmR, smem_u32(sm.cst[warp - kFirstEpi][0]),
                                                      smem_u32(&sm.res_full[warp - kFirstEpi][0]), rphase, pk,
-                                                     nt * pair::BN + half * 128, row0, lane,
+                                                     nt * PBN + half * 128, row0, lane,
                                                      gate_row(ge, row0 + lane))) {
                     if (lane == 0)
                         record_error(ERR_WAIT_ACC);
                     break;
                 }
             } else {
-                store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpi][0]), pk, nt * pair::BN + half * 128, row0, lane);
+                store_rows(&tmC, smem_u32(sm.cst[warp - kFirstEpi][0]), pk, nt * PBN + half * 128, row0, lane);
             }
         }
         if (lane == 0)
@@ -1257,9 +970,9 @@ bool make_scale_map(CUtensorMap *tm, const void *base, int64_t bytes)
     auto fn = encode_fn();
     if (!fn)
         return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(pair::SF_ROW), static_cast<cuuint64_t>(bytes / pair::SF_ROW)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(pair::SF_ROW)};
-    cuuint32_t box[2] = {pair::SF_ROW, 8};
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(paircp::SF_ROW), static_cast<cuuint64_t>(bytes / paircp::SF_ROW)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(paircp::SF_ROW)};
+    cuuint32_t box[2] = {paircp::SF_ROW, 8};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1267,60 +980,11 @@ bool make_scale_map(CUtensorMap *tm, const void *base, int64_t bytes)
     return r == CUDA_SUCCESS;
 }
 
-h3fp4_status launch_pair(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
-                         const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m, int64_t m_pad,
-                         int64_t n, int64_t k, int n_group_cfg, cudaStream_t st)
-{
-    const int64_t sfa_rows = (m_pad + 127) / 128 * 128, sfb_rows = (n + 127) / 128 * 128;
-    CUtensorMap tmA, tmB, tmSFA, tmSFB, tmC;
-    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, pair::BM) || !make_operand_map(&tmB, b_q, n, k / 2, 128) ||
-        !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16)) || !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16)) ||
-        !make_output_map(&tmC, c, m, n, ldc))
-        return H3FP4_ERR_CUDA;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return H3FP4_ERR_CUDA;
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(pair::nvf4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(pair::kSmemBytes)) != cudaSuccess)
-            return H3FP4_ERR_CUDA;
-        attr_set[dev] = true;
-    }
-    const int m_tiles2 = static_cast<int>((m + 255) / 256);
-    const int n_tiles = static_cast<int>((n + pair::BN - 1) / pair::BN);
-    const int64_t total = static_cast<int64_t>(m_tiles2) * n_tiles;
-    if (total > 0x7FFFFFFF)
-        return H3FP4_ERR_SHAPE;
-    int n_group = n_group_cfg > 0 ? n_group_cfg : kDefaultNGroup;
-    if (n_group > n_tiles)
-        n_group = n_tiles;
-    const int max_pairs = sm_count() / 2;
-    const int pairs = static_cast<int>(total < max_pairs ? total : max_pairs);
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(2 * pairs, 1, 1);
-    lc.blockDim = dim3(kThreads, 1, 1);
-    lc.dynamicSmemBytes = pair::kSmemBytes;
-    lc.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&lc, pair::nvf4_gemm_pair_kernel, tmA, tmB, tmSFA, tmSFB, tmC, a_ts, b_ts,
-                                             static_cast<int>(m), static_cast<int>(n), static_cast<int>(k),
-                                             m_tiles2, n_tiles, n_group, static_cast<int>(sfa_rows / 128),
-                                             static_cast<int>(sfb_rows / 128));
-    return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
-}
-
 }  // namespace
 
 namespace {
 
-template <bool kMcast, bool kGated>
+template <bool kGated>
 h3fp4_status launch_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const CUtensorMap &tmR,
                           const GatedEpilogue &ge, const uint8_t *a_sf, const uint8_t *b_sf, const float *a_ts,
                           const float *b_ts, int64_t m, int64_t n, int64_t k, int n_group_cfg, cudaStream_t st)
@@ -1330,45 +994,24 @@ h3fp4_status launch_tiles(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
     if (cudaGetDevice(&dev) != cudaSuccess)
         return H3FP4_ERR_CUDA;
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(nvf4_gemm_kernel<kMcast, kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(nvf4_gemm_kernel<kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes)) != cudaSuccess)
             return H3FP4_ERR_CUDA;
         attr_set[dev] = true;
     }
     const int m_tiles = static_cast<int>((m + BM - 1) / BM);
     const int n_tiles = static_cast<int>((n + BN - 1) / BN);
-    const int m_sched = kMcast ? (m_tiles + 1) / 2 : m_tiles;
-    const int64_t total = static_cast<int64_t>(m_sched) * n_tiles;
+    const int64_t total = static_cast<int64_t>(m_tiles) * n_tiles;
     if (total > 0x7FFFFFFF)
         return H3FP4_ERR_SHAPE;
     int n_group = n_group_cfg > 0 ? n_group_cfg : kDefaultNGroup;
     if (n_group > n_tiles)
         n_group = n_tiles;
-    if (!kMcast) {
-        const int grid = static_cast<int>(total < sm_count() ? total : sm_count());
-        nvf4_gemm_kernel<false, kGated><<<grid, kThreads, kSmemBytes, st>>>(
-            tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, static_cast<int>(m), static_cast<int>(n),
-            static_cast<int>(k), m_tiles, n_tiles, n_group);
-        return cudaGetLastError() == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
-    }
-    const int max_clusters = sm_count() / 2;
-    const int clusters = static_cast<int>(total < max_clusters ? total : max_clusters);
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(2 * clusters, 1, 1);
-    lc.blockDim = dim3(kThreads, 1, 1);
-    lc.dynamicSmemBytes = kSmemBytes;
-    lc.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&lc, nvf4_gemm_kernel<true, kGated>, tmA, tmB, tmC, tmR, ge, a_sf, b_sf,
-                                             a_ts, b_ts, static_cast<int>(m), static_cast<int>(n),
-                                             static_cast<int>(k), m_tiles, n_tiles, n_group);
-    return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
+    const int grid = static_cast<int>(total < sm_count() ? total : sm_count());
+    nvf4_gemm_kernel<kGated><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts,
+                                                                 static_cast<int>(m), static_cast<int>(n),
+                                                                 static_cast<int>(k), m_tiles, n_tiles, n_group);
+    return cudaGetLastError() == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
 }
 
 }  // namespace
@@ -1431,14 +1074,14 @@ h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float
     const int64_t sfa_rows = (m_pad + 127) / 128 * 128, sfb_rows = (n + 127) / 128 * 128;
     CUtensorMap tmA, tmB, tmSFA, tmSFB, tmC, tmR;
     GatedEpilogue ge;
-    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, pair::BM) || !make_operand_map(&tmB, b_q, n, k / 2, 128) ||
+    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, paircp::PBM) || !make_operand_map(&tmB, b_q, n, k / 2, 128) ||
         !make_scale_map(&tmSFA, a_sf, sfa_rows * (k / 16)) || !make_scale_map(&tmSFB, b_sf, sfb_rows * (k / 16)) ||
         !make_output_map(&tmC, c, m, n, ldc) || !make_gated(gated, tmC, m, n, &tmR, &ge))
         return H3FP4_ERR_CUDA;
     if ((gated ? set_pair_cp_smem<true>() : set_pair_cp_smem<false>()) != cudaSuccess)
         return H3FP4_ERR_CUDA;
     const int m_tiles2 = static_cast<int>((m + 255) / 256);
-    const int n_tiles = static_cast<int>((n + pair::BN - 1) / pair::BN);
+    const int n_tiles = static_cast<int>((n + paircp::PBN - 1) / paircp::PBN);
     const int64_t total = static_cast<int64_t>(m_tiles2) * n_tiles;
     if (total > 0x7FFFFFFF)
         return H3FP4_ERR_SHAPE;
@@ -1477,23 +1120,15 @@ h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a
         return H3FP4_OK;
     if (cfg.cta_pair == 0 || cfg.cta_pair == 4)   // the default: measured fastest in the DiT step
         return launch_pair_cp(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, gated, st);
-    if (cfg.cta_pair == 2) {
-        if (gated != nullptr)
-            return H3FP4_ERR_UNSUPPORTED;
-        return launch_pair(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, cfg.n_group, st);
-    }
-    const bool mcast = cfg.cta_pair == 3;
+    if (cfg.cta_pair != 1)
+        return H3FP4_ERR_UNSUPPORTED;
     CUtensorMap tmA, tmB, tmC, tmR;
     GatedEpilogue ge;
-    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, BM) ||
-        !make_operand_map(&tmB, b_q, n, k / 2, mcast ? BN / 2 : BN) || !make_output_map(&tmC, c, m, n, ldc) ||
-        !make_gated(gated, tmC, m, n, &tmR, &ge))
+    if (!make_operand_map(&tmA, a_q, m_pad, k / 2, BM) || !make_operand_map(&tmB, b_q, n, k / 2, BN) ||
+        !make_output_map(&tmC, c, m, n, ldc) || !make_gated(gated, tmC, m, n, &tmR, &ge))
         return H3FP4_ERR_CUDA;
-    if (mcast)
-        return gated ? launch_tiles<true, true>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st)
-                     : launch_tiles<true, false>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st);
-    return gated ? launch_tiles<false, true>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st)
-                 : launch_tiles<false, false>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st);
+    return gated ? launch_tiles<true>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st)
+                 : launch_tiles<false>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st);
 }
 
 h3fp4_status read_device_error(uint32_t *code)

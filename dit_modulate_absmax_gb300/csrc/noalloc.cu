@@ -14,7 +14,9 @@
 // Set-up: the array's device address is looked up once per device (with
 // that device current) by cudaGetSymbolAddress on the first call made on it;
 // that first call may also load this file's device module, so it should come
-// before any stream capture.
+// before any stream capture.  The address is kept for the life of the
+// process's context on that device: a caller that destroys the context
+// (cudaDeviceReset) must not call this entry point again in that process.
 //
 // Sharing: every call uses the same array and it keeps the last call's
 // contents.  The two counter words are cleared on the stream by every call;
@@ -70,7 +72,7 @@ extern "C" h3fp4_status h3fp4_swiglu_pack_noalloc(const void *gate_bf16, int64_t
         sfa == nullptr)
         return H3FP4_ERR_NULL;
     if (m < 0 || m > INT32_MAX || f <= 0 || f % 256 != 0 || f > (int64_t(1) << 24) || ldg < f || ldu < f ||
-        m_pad < m || m_pad > INT32_MAX)
+        m_pad < m || m_pad % 16 != 0 || m_pad > INT32_MAX)
         return H3FP4_ERR_SHAPE;
     if (m * f > kMaxH)
         return H3FP4_ERR_SHAPE;  // h would not fit the static workspace

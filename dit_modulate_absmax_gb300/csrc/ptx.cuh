@@ -113,29 +113,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
-// Multicast forms: the data lands at this shared offset in every CTA of the
-// cluster named in `mask`, and each destination CTA's mbarrier at offset `bar`
-// receives the complete_tx of its copy.
-__device__ __forceinline__ void tma_load_2d_mcast(uint32_t dst, const void *tmap, int32_t x, int32_t y, uint32_t bar,
-                                                  uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_load_mcast(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
-                                                uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "h"(mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -177,13 +154,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
            (static_cast<uint64_t>(layout & 7u) << 61);
 }
 
-// Copies a 32-row x 16-byte block of shared memory (one 512-byte scale atom)
-// into 4 TMEM columns, replicated into all four 32-lane quarters.
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // D (TMEM, FP32) (+)= A (smem desc) x B (smem desc), E2M1 operands with UE4M3
 // scales, one scale per 16 K-elements (4 per row per instruction, K = 64).
 __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -198,69 +168,12 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
-// Warp-collective forms of the tcgen05 issue: the whole warp executes the
-// instruction and one lane (elect.sync: the lowest active lane) issues it, so
-// the operands stay warp-uniform.  Issued from a one-lane branch instead, each
-// tcgen05 instruction measured ~30 cycles of extra issue cost, enough to make
-// 12 scale-atom copies per K step cost 370 cycles on top of the 4 MMAs; issued
-// warp-collectively they run under the MMAs for free.  All lanes of the warp
-// must be active; the issuing lane is then lane 0 for every call, so that a
-// later commit from lane 0 (or from tc_commit_elect) covers these operations.
-__device__ __forceinline__ void tc_cp_32x128b_warpx4_elect(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
-        "@p tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
-        "l"(sdesc)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_mma_nvf4_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.b32 q, %6, 0;\n\t"
-        "elect.sync _|p, 0xffffffff;\n\t"
-        "@p tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit_elect(uint32_t bar)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
-        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit_mc_elect(uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
-        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
-
 // Arrives once on the mbarrier when all previously issued tcgen05 async
 // operations of this thread have completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// As tc_commit, but the arrival goes to the mbarrier at this shared offset in
-// every CTA of the cluster named in `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
 }
 
 // 32 lanes x 32 columns of 32-bit TMEM words: thread t of the warp receives the
@@ -416,30 +329,18 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 
-// Scale atom copy for a CTA pair (issued by the pair's MMA thread): each CTA's
-// atom at this shared address goes to the same TMEM columns of that CTA.
-__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// Pair MMA: M = 256 rows (128 from each CTA's shared memory at the same
-// address), N columns (N/2 B rows from each CTA), each CTA accumulating its
-// 128 rows x N in its own TMEM.
-__device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-// Warp-collective (elect.sync) forms of the pair copy, MMA and commit; see
-// tc_cp_32x128b_warpx4_elect.
+// Warp-collective forms of the pair's tcgen05 issue: the whole warp executes
+// the instruction and one lane (elect.sync: the lowest active lane) issues it,
+// so the operands stay warp-uniform.  Issued from a one-lane branch instead,
+// each tcgen05 instruction measured ~30 cycles of extra issue cost, enough to
+// make 12 scale-atom copies per K step cost 370 cycles on top of the MMAs;
+// issued warp-collectively they run under the MMAs for free.  All lanes of the
+// warp must be active; the issuing lane is then lane 0 for every call, so that
+// a later commit from the same warp covers these operations.
+//
+// Scale atom copy: each CTA's 32-row x 16-byte block at this shared address
+// goes to the same TMEM columns of that CTA, replicated into all four 32-lane
+// quarters.
 __device__ __forceinline__ void tc_cp_32x128b_warpx4_pair_elect(uint32_t taddr, uint64_t sdesc)
 {
     asm volatile(
@@ -449,6 +350,10 @@ __device__ __forceinline__ void tc_cp_32x128b_warpx4_pair_elect(uint32_t taddr, 
         : "memory");
 }
 
+// Pair MMA: M = 256 rows (128 from each CTA's shared memory at the same
+// address), N columns (N/2 B rows from each CTA), each CTA accumulating its
+// 128 rows x N in its own TMEM.  E2M1 operands with UE4M3 scales, one scale
+// per 16 K-elements; K = 64 or, with instruction-descriptor bit 31, 96.
 __device__ __forceinline__ void tc_mma_nvf4_pair_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
                                                        uint32_t accumulate)
@@ -463,21 +368,14 @@ __device__ __forceinline__ void tc_mma_nvf4_pair_elect(uint32_t d_tmem, uint64_t
         : "memory");
 }
 
+// Arrives once on the mbarrier at this shared offset in every CTA of `mask`
+// when the pair's previously issued tcgen05 operations have completed (an
+// mbarrier signal, not a data copy).
 __device__ __forceinline__ void tc_commit_pair_mc_elect(uint32_t bar, uint16_t mask)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
         "@p tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
-
-// Arrives once on the mbarrier at this shared offset in every CTA of `mask`
-// when the pair's previously issued tcgen05 operations have completed.
-__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
         "h"(mask)
         : "memory");
 }

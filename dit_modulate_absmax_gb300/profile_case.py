@@ -32,8 +32,8 @@ def main():
     ap.add_argument("--k", type=int, default=7168)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--cta-pair", type=int, default=0,
-                    help="GEMM kernel (h3fp4_gemm_config.cta_pair): 0 default, 1 single CTA, 2 CTA pair with scale "
-                         "warps, 3 two-CTA multicast cluster, 4 CTA pair with copied scales")
+                    help="GEMM kernel (h3fp4_gemm_config.cta_pair): 0 default, 1 single CTA, "
+                         "4 CTA pair with copied scales")
     ap.add_argument("--n-group", type=int, default=0, help="GEMM N-group (0 = default)")
     ap.add_argument("--single-launch", action="store_true",
                     help="modulate: both passes in one cooperative launch (h3fp4_modulate_produce)")

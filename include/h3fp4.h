@@ -188,14 +188,11 @@ typedef struct h3fp4_gemm_config {
     int32_t n_group;
     int32_t stages;    /* reserved, must be 0 (the pipeline depth is fixed per kernel) */
     /* GEMM kernel: 0 = library default (currently 4), 1 = one CTA per 128 x 256 output tile
-     * (4-stage ring, scale warps stage the scales in TMEM), 2 = CTA pairs on
-     * two SMs per 256 x 256 tile (tcgen05 cta_group::2, each SM loads half of
-     * A and half of B; 6-stage ring; scale warps; no gated epilogue), 3 =
-     * clusters of two CTAs on the two 128 x 256 tiles of one 256 x 256 block,
-     * each loading its own A and half of the shared B tile, multicast into
-     * both (4-stage ring, scale warps), 4 = CTA pairs as 2 whose leader
-     * copies the scales into TMEM with tcgen05.cp from a warp of its own
-     * (5-stage ring). */
+     * (4-stage ring, scale warps stage the scales in TMEM), 4 = CTA pairs on
+     * two SMs per 256 x 256 tile (tcgen05 cta_group::2, each SM loads its own
+     * half of A and of B; 5-stage ring) whose leader copies the scales into
+     * TMEM with tcgen05.cp from two warps of their own.  Other values:
+     * H3FP4_ERR_UNSUPPORTED. */
     int32_t cta_pair;
     int32_t reserved;  /* must be 0 */
 } h3fp4_gemm_config;
@@ -243,7 +240,7 @@ H3FP4_API h3fp4_status h3fp4_gemm(const uint8_t *a_q, const uint8_t *a_sf, const
  *   residual_bf16  [m, n] bf16, leading dimension ldr (>= n, multiple of 8), 16-byte aligned
  *   out_bf16       [m, n] bf16, leading dimension ldo; either the residual itself (same pointer and
  *                  leading dimension: updated in place) or not overlapping it (else H3FP4_ERR_UNSUPPORTED)
- *   other arguments as for h3fp4_gemm; cfg->cta_pair = 2 is not supported (H3FP4_ERR_UNSUPPORTED)
+ *   other arguments as for h3fp4_gemm
  */
 H3FP4_API h3fp4_status h3fp4_gemm_gated_residual(
     const uint8_t *a_q, const uint8_t *a_sf, const float *a_tensor_scale, const uint8_t *b_q, const uint8_t *b_sf,

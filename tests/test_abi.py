@@ -84,6 +84,7 @@ def test_modulate_pack_validation(L):
     f = L.h3fp4_modulate_pack
     off = _offs(0, 10)
     assert f(F, 256, 10, 8, 256, F, F, 256, off, 1, F, F, F, None) == SHAPE        # m_pad < m
+    assert f(F, 256, 10, 24, 256, F, F, 256, off, 1, F, F, F, None) == SHAPE       # m_pad not a multiple of 16
     assert f(F, 256, 10, 16, 256, F, F, 256, off, 1, None, F, F, None) == NULL
     assert f(F, 256, 10, 16, 256, F, F, 256, off, 1, F, None, F, None) == NULL
     assert f(F, 256, 10, 16, 256, F, F, 256, off, 1, F, F, F + 4, None) == ALIGN
@@ -95,6 +96,17 @@ def test_swiglu_pack_validation(L):
     assert f(F, 256, F, 256, 10, 16, 300, F, F, F, F, None, None) == SHAPE
     assert f(F, 256, F, 256, 10, 16, 256, F, F, F, F, F + 2, None) == ALIGN
     assert f(F, 256, F, 256, 10, 4, 256, F, F, F, F, None, None) == SHAPE
+    assert f(F, 256, F, 256, 10, 20, 256, F, F, F, F, None, None) == SHAPE      # m_pad not a multiple of 16
+
+
+def test_swiglu_pack_noalloc_validation(L):
+    f = L.h3fp4_swiglu_pack_noalloc
+    assert f(None, 256, F, 256, 10, 16, 256, F, F, F, None) == NULL
+    assert f(F, 256, F, 256, 10, 16, 300, F, F, F, None) == SHAPE               # f not a multiple of 256
+    assert f(F, 256, F, 256, 10, 4, 256, F, F, F, None) == SHAPE                # m_pad < m
+    assert f(F, 256, F, 256, 10, 20, 256, F, F, F, None) == SHAPE               # m_pad not a multiple of 16
+    big = pkg.NOALLOC_MAX_ELEMENTS // 256 + 1
+    assert f(F, 256, F, 256, big, -(-big // 16) * 16, 256, F, F, F, None) == SHAPE   # beyond the static scratch
 
 
 def test_modulate_produce_validation(L):
@@ -104,6 +116,7 @@ def test_modulate_produce_validation(L):
     assert f(F, 256, 10, 16, 256, F, F, 256, offs, 1, None, F, F, F, None) == NULL     # tensor scale
     assert f(F, 256, 10, 16, 300, F, F, 256, offs, 1, F, F, F, F, None) == SHAPE
     assert f(F, 256, 10, 4, 256, F, F, 256, offs, 1, F, F, F, F, None) == SHAPE       # m_pad < m
+    assert f(F, 256, 10, 40, 256, F, F, 256, offs, 1, F, F, F, F, None) == SHAPE      # m_pad not a multiple of 16
     assert f(F, 256, 10, 16, 256, F, F, 256, (ctypes.c_int32 * 2)(0, 9), 1, F, F, F, F, None) == SHAPE
 
 
@@ -114,6 +127,7 @@ def test_quantize_pack_validation(L):
     assert f(F, 200, 10, 16, 256, F, F, F, F, None) == SHAPE       # ldx < d
     assert f(F + 2, 256, 10, 16, 256, F, F, F, F, None) == ALIGN
     assert f(F, 256, 10, 4, 256, F, F, F, F, None) == SHAPE         # m_pad < m
+    assert f(F, 256, 10, 17, 256, F, F, F, F, None) == SHAPE        # m_pad not a multiple of 16
 
 
 def test_gemm_validation(L):
@@ -134,8 +148,9 @@ def test_gemm_validation(L):
     assert call(cfg=ctypes.byref(bad)) == UNSUP
     bad = pkg.GemmConfig(0, 3, 0, 0)
     assert call(cfg=ctypes.byref(bad)) == UNSUP
-    bad = pkg.GemmConfig(0, 0, 5, 0)       # kernels are 0 (default) .. 4
-    assert call(cfg=ctypes.byref(bad)) == UNSUP
+    for kernel in (2, 3, 5):               # kernels are 0 (default), 1 and 4
+        bad = pkg.GemmConfig(0, 0, kernel, 0)
+        assert call(cfg=ctypes.byref(bad)) == UNSUP
 
 
 def test_gemm_gated_residual_validation(L):
@@ -153,7 +168,7 @@ def test_gemm_gated_residual_validation(L):
     assert call(ldr=388) == ALIGN
     assert call(off=(ctypes.c_int32 * 3)(0, 250, 200)) == SHAPE          # offsets must not decrease
     assert call(residual=F + 64) == UNSUP                                 # partial overlap with the output
-    assert call(cfg=ctypes.byref(pkg.GemmConfig(0, 0, 2, 0))) == UNSUP     # the scale-warp pair kernel has no gated form
+    assert call(cfg=ctypes.byref(pkg.GemmConfig(0, 0, 3, 0))) == UNSUP     # no such kernel
 
 
 def test_swizzle_and_device_error_validation(L):

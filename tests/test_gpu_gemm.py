@@ -16,11 +16,10 @@ from dit_modulate_absmax_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 CANARY16 = 0x7E7E
 
-# Every GEMM kernel: one CTA per 128 x 256 tile (cta_pair=1), CTA pairs on
-# 256 x 256 tiles with scale warps (cta_pair=2), two-CTA clusters sharing B
-# by multicast (cta_pair=3), and CTA pairs with the scales copied into TMEM
-# by the MMA warp (cta_pair=4, the default).
-KERNELS = {"single": 1, "pair": 2, "mcast": 3, "pair_cp": 4}
+# Every GEMM kernel: one CTA per 128 x 256 tile (cta_pair=1) and CTA pairs on
+# 256 x 256 tiles with the scales copied into TMEM by copy warps (cta_pair=4,
+# the default).
+KERNELS = {"single": 1, "pair_cp": 4}
 
 
 @pytest.fixture(params=sorted(KERNELS), ids=sorted(KERNELS))
@@ -168,7 +167,7 @@ def test_scale_atom_rows_are_not_mixed(h3, cfg):
 # ---------------------------------------------------------------------------
 # Gated residual epilogue ("NVFP4 Streaming Design", P4)
 # ---------------------------------------------------------------------------
-GATED_KERNELS = {"single": 1, "mcast": 3, "pair_cp": 4}
+GATED_KERNELS = {"single": 1, "pair_cp": 4}
 
 
 def _gated_inputs(rng, m, n, nseg):

@@ -71,11 +71,12 @@ def test_noalloc_matches_swiglu_pack_on_two_calls_in_a_row(h3):
 def test_noalloc_rejects_problems_beyond_its_static_scratch(h3):
     f = 1024
     m = h3.NOALLOC_MAX_ELEMENTS // f + 1
+    m_pad = -(-m // 16) * 16                   # a valid padding: only the size limit is broken
     gate, up = _inputs(16, f, 3, 1.0)          # real buffers; the size check fails before any use
     ts, q, sfa = _outputs(h3, 16, f)
     with pytest.raises(h3.H3FP4Error) as e:
-        h3.h3fp4_swiglu_pack_noalloc(gate.data_ptr(), f, up.data_ptr(), f, m, m, f, ts.data_ptr(), q.data_ptr(),
-                                     sfa.data_ptr(), _stream())
+        h3.h3fp4_swiglu_pack_noalloc(gate.data_ptr(), f, up.data_ptr(), f, m, m_pad, f, ts.data_ptr(),
+                                     q.data_ptr(), sfa.data_ptr(), _stream())
     assert e.value.status == 3                 # H3FP4_ERR_SHAPE
     torch.cuda.synchronize()
     assert torch.isnan(ts).all() and (q == 0xAB).all() and (sfa == 0xAB).all()
