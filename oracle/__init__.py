@@ -56,13 +56,16 @@ SF_ROW_TILE = 128
 
 
 def build(force: bool = False) -> str:
-    """Compile the C oracle (gcc, no fast-math, no FMA contraction)."""
+    """Compile the C oracle (gcc, no fast-math, no FMA contraction), with
+    OpenMP over rows where the compiler supports it (serial otherwise)."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".{os.getpid()}.tmp"
-        subprocess.check_call([
-            "gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-            "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
+        base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+        try:
+            subprocess.check_call(base + ["-fopenmp", "-o", tmp, _SRC, "-lm"], stderr=subprocess.DEVNULL)
+        except subprocess.CalledProcessError:
+            subprocess.check_call(base + ["-Wno-unknown-pragmas", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -111,7 +114,20 @@ def lib() -> ctypes.CDLL:
     L.orc_unswizzle_sf.argtypes = [_P, _I64, _I64, _P]
     L.orc_dequant.restype = None
     L.orc_dequant.argtypes = [_P, _P, _I64, ctypes.c_float, _I64, _I64, _P]
+    L.orc_set_threads.restype = None
+    L.orc_set_threads.argtypes = [ctypes.c_int]
+    L.orc_threads.restype = ctypes.c_int
+    L.orc_threads.argtypes = []
     return L
+
+
+def set_threads(n: int) -> None:
+    """Threads for the C row loops (1 = the plain serial oracle)."""
+    lib().orc_set_threads(int(n))
+
+
+def threads() -> int:
+    return int(lib().orc_threads())
 
 
 def _ptr(a: np.ndarray) -> int:

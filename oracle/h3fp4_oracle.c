@@ -37,6 +37,33 @@
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------------------
+ * Threads.  When built with OpenMP the row loops below run their rows on
+ * several threads; each row's arithmetic is exactly the same whichever thread
+ * runs it, and the only cross-row step (the absolute maximum) is an exact,
+ * order-independent max.  Without OpenMP everything runs on one thread.
+ * ------------------------------------------------------------------------- */
+void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}
+
+int orc_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ---------------------------------------------------------------------------
  * Generic rounding: round finite v to the nearest value of a binary format with
@@ -159,6 +186,7 @@ void orc_modulate(const uint16_t *x, int64_t ldx, int64_t m, int64_t d,
                   const int32_t *seg_off, int32_t nseg,
                   uint16_t *y, int64_t ldy)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < m; ++r) {
         int32_t s = 0;
         while (s + 1 < nseg && r >= seg_off[s + 1])
@@ -189,6 +217,7 @@ void orc_gated_residual(const uint16_t *c, int64_t ldc, const uint16_t *gate, in
                         const int32_t *seg_off, int32_t nseg, const uint16_t *res, int64_t ldr,
                         int64_t m, int64_t n, uint16_t *out, int64_t ldo)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < m; ++r) {
         int32_t s = 0;
         while (s + 1 < nseg && r >= seg_off[s + 1])
@@ -213,6 +242,7 @@ void orc_swiglu(const uint16_t *g, int64_t ldg, const uint16_t *u, int64_t ldu,
                 int64_t m, int64_t f, const uint16_t *silu_table,
                 uint16_t *h, int64_t ldh)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < m; ++r)
         for (int64_t j = 0; j < f; ++j) {
             double sg = orc_bf16_value(silu_table[g[r * ldg + j]]);
@@ -230,6 +260,7 @@ uint16_t orc_absmax(const uint16_t *y, int64_t ldy, int64_t m, int64_t d)
 {
     double amax = 0.0;
     int nan = 0;
+#pragma omp parallel for schedule(static) reduction(max : amax) reduction(| : nan)
     for (int64_t r = 0; r < m; ++r)
         for (int64_t j = 0; j < d; ++j) {
             double v = orc_bf16_value(y[r * ldy + j]);
@@ -263,6 +294,7 @@ void orc_pack(const uint16_t *y, int64_t ldy, int64_t m, int64_t m_pad, int64_t 
     memset(sf, 0, (size_t)(sf_rows * nb));
     double tsd = (double)ts;
     double den = orc_rn_f32(6.0 * tsd);
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < m; ++r)
         for (int64_t b = 0; b < nb; ++b) {
             double v[16], bamax = 0.0;
@@ -306,6 +338,7 @@ int64_t orc_sf_offset(int64_t r, int64_t c, int64_t cols)
 
 void orc_swizzle_sf(const uint8_t *sf, int64_t rows, int64_t cols, uint8_t *out)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c)
             out[orc_sf_offset(r, c, cols)] = sf[r * cols + c];
@@ -313,6 +346,7 @@ void orc_swizzle_sf(const uint8_t *sf, int64_t rows, int64_t cols, uint8_t *out)
 
 void orc_unswizzle_sf(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *sf)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c)
             sf[r * cols + c] = in[orc_sf_offset(r, c, cols)];
@@ -323,6 +357,7 @@ void orc_unswizzle_sf(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *sf
 void orc_dequant(const uint8_t *q, const uint8_t *sf, int64_t k, float ts,
                  int64_t r0, int64_t r1, double *out)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = r0; r < r1; ++r)
         for (int64_t j = 0; j < k; ++j) {
             uint8_t byte = q[r * (k / 2) + j / 2];
