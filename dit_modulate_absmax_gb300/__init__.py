@@ -35,6 +35,10 @@ _SIGNATURES = {
     "h3fp4_swizzle_scales": ([_P, _I64, _I64, _I64, _P, _P], _STATUS),
     "h3fp4_swiglu_pack_noalloc": ([_P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P], _STATUS),
     "h3fp4_device_error": ([_P], _STATUS),
+    "h3fp4_diag_producer_barrier_timeout": ([_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_uint32, _P],
+                                            _STATUS),
+    "h3fp4_diag_gemm_wait_timeout": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, ctypes.c_uint32, _P],
+                                     _STATUS),
     "h3fp4_status_string": ([_STATUS], ctypes.c_char_p),
     "h3fp4_build_info": ([], ctypes.c_char_p),
 }
@@ -149,6 +153,17 @@ def h3fp4_device_error() -> int:
     code = ctypes.c_uint32(0)
     _call("h3fp4_device_error", ctypes.byref(code))
     return code.value
+
+
+def h3fp4_diag_producer_barrier_timeout(x, ldx, m, m_pad, d, tensor_scale, scratch, qdata, sfa, limit_us, stream=0):
+    """Failure-detection check: the cooperative producer's grid barrier gives up after limit_us."""
+    _call("h3fp4_diag_producer_barrier_timeout", x, ldx, m, m_pad, d, tensor_scale, scratch, qdata, sfa, limit_us,
+          stream)
+
+
+def h3fp4_diag_gemm_wait_timeout(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, limit_us, stream=0):
+    """Failure-detection check: the default GEMM with its loads withheld; its waits give up after limit_us."""
+    _call("h3fp4_diag_gemm_wait_timeout", a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, limit_us, stream)
 
 
 def h3fp4_build_info() -> str:

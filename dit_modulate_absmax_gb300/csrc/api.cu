@@ -253,6 +253,42 @@ h3fp4_status h3fp4_swizzle_scales(const uint8_t *sf_logical, int64_t rows, int64
     return from_cuda(h3fp4::launch_swizzle_scales(sf_logical, rows, cols, ld, sf_out, as_stream(stream)));
 }
 
+h3fp4_status h3fp4_diag_producer_barrier_timeout(const void *x_bf16, int64_t ldx, int64_t m, int64_t m_pad,
+                                                 int64_t d, float *tensor_scale, uint32_t *scratch, uint8_t *qdata,
+                                                 uint8_t *sfa, uint32_t limit_us, void *stream)
+{
+    if ((x_bf16 == nullptr && m != 0) || tensor_scale == nullptr || scratch == nullptr)
+        return H3FP4_ERR_NULL;
+    if (m < 0 || m > INT32_MAX || d <= 0 || d % 256 != 0 || d > (int64_t(1) << 24) || ldx < d || limit_us == 0 ||
+        limit_us > 2000000u)
+        return H3FP4_ERR_SHAPE;
+    if (!aligned16(x_bf16) || ldx % 8 != 0)
+        return H3FP4_ERR_ALIGN;
+    h3fp4_status s = check_pack_outputs(m, m_pad, qdata, sfa);
+    if (s != H3FP4_OK)
+        return s;
+    return from_cuda(h3fp4::launch_quantize_pack_barrier_timeout(
+        static_cast<const uint16_t *>(x_bf16), ldx, m, m_pad, d, tensor_scale, scratch, qdata, sfa,
+        static_cast<uint64_t>(limit_us) * 1000u, as_stream(stream)));
+}
+
+h3fp4_status h3fp4_diag_gemm_wait_timeout(const uint8_t *a_q, const uint8_t *a_sf, const float *a_tensor_scale,
+                                          const uint8_t *b_q, const uint8_t *b_sf, const float *b_tensor_scale,
+                                          void *c_bf16, int64_t ldc, int64_t m, int64_t m_pad, int64_t n, int64_t k,
+                                          uint32_t limit_us, void *stream)
+{
+    h3fp4_gemm_config c;
+    h3fp4_status s = check_gemm(a_q, a_sf, a_tensor_scale, b_q, b_sf, b_tensor_scale, c_bf16, ldc, m, m_pad, n, k,
+                                nullptr, &c);
+    if (s != H3FP4_OK)
+        return s;
+    if (limit_us == 0 || limit_us > 2000000u)
+        return H3FP4_ERR_SHAPE;
+    return h3fp4::launch_gemm_wait_timeout(a_q, a_sf, a_tensor_scale, b_q, b_sf, b_tensor_scale,
+                                           static_cast<uint16_t *>(c_bf16), ldc, m, m_pad, n, k,
+                                           static_cast<uint64_t>(limit_us) * 1000u, as_stream(stream));
+}
+
 h3fp4_status h3fp4_device_error(uint32_t *code)
 {
     if (code == nullptr)

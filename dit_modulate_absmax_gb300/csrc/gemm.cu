@@ -134,11 +134,11 @@ static_assert(stage_mma_k0(1) + 96 <= stage_mma_k0(2) && stage_mma_k0(2) + 64 ==
 __device__ __forceinline__ void record_error(uint32_t code) { atomicOr(&g_device_error, code); }
 
 // Bounded wait on behalf of a whole warp; the outcome is warp-uniform.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs)
 {
     // Every lane polls: polling from lane 0 alone and broadcasting the outcome
     // measured 4-13% slower (a later wake-up of the other lanes).
-    const bool ok = mbar_wait_bounded(bar, parity, kWaitLimitNs);
+    const bool ok = mbar_wait_bounded(bar, parity, limit_ns);
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -146,13 +146,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
 // suspending try_wait: for a warp whose wake-up latency sits on the critical
 // path (the default GEMM's MMA warp: 1.2 % faster), at the price of issue
 // slots while it spins.  Bounded like every other wait.
-__device__ __forceinline__ bool warp_wait_spin(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool warp_wait_spin(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs)
 {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (__all_sync(0xFFFFFFFFu, mbar_test_wait(bar, parity)))
             return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs)
+        if (globaltimer_ns() - t0 > limit_ns)
             return false;
     }
 }
@@ -379,7 +379,10 @@ __device__ __forceinline__ bool store_rows_gated_ring(const CUtensorMap *tmC, co
 }
 
 // Output tile t of the persistent schedule: groups of n_group N-tiles x all
-// M-tiles, N fastest inside a group (the last group may be narrower).
+// M-tiles, N fastest inside a group (the last group may be narrower).  Odd
+// groups sweep M backwards, so that a group starts on the A row blocks the
+// previous one read last, still partly in L2 (full QKV: DRAM reads 607 ->
+// 592 MB per launch, same time).
 __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int n_group, int &mt, int &nt)
 {
     const int group_tiles = n_group * m_tiles;
@@ -388,6 +391,8 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
     const int ng = min(n_group, n_tiles - g * n_group);
     nt = g * n_group + tt % ng;
     mt = tt / ng;
+    if (g & 1)
+        mt = m_tiles - 1 - mt;
 }
 
 // One CTA per 128 x 256 output tile: warp 0 loads A, B and their scale atoms
@@ -681,7 +686,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                              const __grid_constant__ GatedEpilogue ge, const float *__restrict__ a_ts,
                              const float *__restrict__ b_ts, int m, int n, int k, int m_tiles2, int n_tiles,
-                             int n_group)
+                             int n_group, uint64_t wait_ns, int withhold_loads)
 {
     using G = Geo;
     constexpr int kStages = G::kStages;
@@ -725,7 +730,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) {
+        // withhold_loads (failure-detection entry point only): no copy is issued,
+        // so every wait of the other warps runs out after wait_ns
+        if (lane == 0 && !withhold_loads) {
             uint32_t it = 0;
             bool ok = true;
             for (int t = pair_id; t < total_tiles && ok; t += num_pairs) {
@@ -734,7 +741,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 const int rb_a = 2 * mt2 + static_cast<int>(rank);
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
-                    if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ((it / kStages) & 1) ^ 1u, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ((it / kStages) & 1) ^ 1u, wait_ns)) {
                         record_error(ERR_WAIT_EMPTY);
                         ok = false;
                         break;
@@ -774,7 +781,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             for (int t = pair_id; t < total_tiles && ok; t += num_pairs) {
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
-                    if (!warp_wait(smem_u32(&sm.sf_full[s]), (it / kStages) & 1)) {
+                    if (!warp_wait(smem_u32(&sm.sf_full[s]), (it / kStages) & 1, wait_ns)) {
                         if (lane == 0)
                             record_error(ERR_WAIT_SCALES);
                         ok = false;
@@ -810,7 +817,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             bool ok = true;
             bool known_ready = false;   // the current stage's barrier was seen complete during the previous stage
             for (int t = pair_id; t < total_tiles && ok; t += num_pairs, ++local) {
-                if (!warp_wait(smem_u32(&sm.acc_empty), (local & 1) ^ 1u)) {
+                if (!warp_wait(smem_u32(&sm.acc_empty), (local & 1) ^ 1u, wait_ns)) {
                     if (lane == 0)
                         record_error(ERR_WAIT_ACC_EMPTY);
                     break;
@@ -818,7 +825,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 tc_fence_after();
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = it % kStages;
-                    if (!known_ready && !warp_wait_spin(smem_u32(&sm.full[s]), (it / kStages) & 1)) {
+                    if (!known_ready && !warp_wait_spin(smem_u32(&sm.full[s]), (it / kStages) & 1, wait_ns)) {
                         if (lane == 0)
                             record_error(ERR_WAIT_FULL);
                         ok = false;
@@ -860,7 +867,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         for (int t = pair_id; t < total_tiles; t += num_pairs, ++local) {
             int mt2, nt;
             tile_coords(t, m_tiles2, n_tiles, n_group, mt2, nt);
-            if (!warp_wait(smem_u32(&sm.acc_full), local & 1)) {
+            if (!warp_wait(smem_u32(&sm.acc_full), local & 1, wait_ns)) {
                 if (lane == 0)
                     record_error(ERR_WAIT_ACC);
                 break;
@@ -1069,7 +1076,7 @@ int pair_default_n_group(int n_tiles, int64_t k)
 h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts, const uint8_t *b_q,
                             const uint8_t *b_sf, const float *b_ts, uint16_t *c, int64_t ldc, int64_t m,
                             int64_t m_pad, int64_t n, int64_t k, int n_group_cfg, const GatedArgs *gated,
-                            cudaStream_t st)
+                            cudaStream_t st, uint64_t wait_ns = kWaitLimitNs, int withhold_loads = 0)
 {
     const int64_t sfa_rows = (m_pad + 127) / 128 * 128, sfb_rows = (n + 127) / 128 * 128;
     CUtensorMap tmA, tmB, tmSFA, tmSFB, tmC, tmR;
@@ -1105,10 +1112,10 @@ h3fp4_status launch_pair_cp(const uint8_t *a_q, const uint8_t *a_sf, const float
     const cudaError_t e =
         gated ? cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<true>, tmA, tmB, tmSFA, tmSFB, tmC, tmR,
                                    ge, a_ts, b_ts, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k),
-                                   m_tiles2, n_tiles, n_group)
+                                   m_tiles2, n_tiles, n_group, wait_ns, withhold_loads)
               : cudaLaunchKernelEx(&lc, paircp::nvf4_gemm_pair_cp_kernel<false>, tmA, tmB, tmSFA, tmSFB, tmC, tmR, ge,
                                    a_ts, b_ts, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), m_tiles2,
-                                   n_tiles, n_group);
+                                   n_tiles, n_group, wait_ns, withhold_loads);
     return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
 }
 
@@ -1129,6 +1136,16 @@ h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a
         return H3FP4_ERR_CUDA;
     return gated ? launch_tiles<true>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st)
                  : launch_tiles<false>(tmA, tmB, tmC, tmR, ge, a_sf, b_sf, a_ts, b_ts, m, n, k, cfg.n_group, st);
+}
+
+h3fp4_status launch_gemm_wait_timeout(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts,
+                                      const uint8_t *b_q, const uint8_t *b_sf, const float *b_ts, uint16_t *c,
+                                      int64_t ldc, int64_t m, int64_t m_pad, int64_t n, int64_t k, uint64_t wait_ns,
+                                      cudaStream_t st)
+{
+    if (m == 0 || n == 0)
+        return H3FP4_OK;
+    return launch_pair_cp(a_q, a_sf, a_ts, b_q, b_sf, b_ts, c, ldc, m, m_pad, n, k, 0, nullptr, st, wait_ns, 1);
 }
 
 h3fp4_status read_device_error(uint32_t *code)

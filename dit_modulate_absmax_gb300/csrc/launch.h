@@ -57,6 +57,19 @@ h3fp4_status launch_gemm(const uint8_t *a_q, const uint8_t *a_sf, const float *a
                          int64_t m_pad, int64_t n, int64_t k, const h3fp4_gemm_config &cfg, const GatedArgs *gated,
                          cudaStream_t st);
 
+// Failure detection (diagnostics, not the hot path): the default GEMM with its
+// operand loads withheld, so that every consumer wait runs out after wait_ns;
+// the cooperative plain producer with a grid-barrier arrival target the grid
+// cannot meet and a barrier limit of wait_ns.  Outputs are left untouched; the
+// kernels record device error bits and return.
+h3fp4_status launch_gemm_wait_timeout(const uint8_t *a_q, const uint8_t *a_sf, const float *a_ts,
+                                      const uint8_t *b_q, const uint8_t *b_sf, const float *b_ts, uint16_t *c,
+                                      int64_t ldc, int64_t m, int64_t m_pad, int64_t n, int64_t k, uint64_t wait_ns,
+                                      cudaStream_t st);
+cudaError_t launch_quantize_pack_barrier_timeout(const uint16_t *x, int64_t ldx, int64_t m, int64_t m_pad,
+                                                int64_t d, float *ts, uint32_t *scratch, uint8_t *qdata, uint8_t *sf,
+                                                uint64_t wait_ns, cudaStream_t st);
+
 h3fp4_status read_device_error(uint32_t *code);
 
 }  // namespace h3fp4

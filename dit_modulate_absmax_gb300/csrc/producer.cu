@@ -587,6 +587,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks<Src>()) pack_kernel(Src s
 // itself and claims pass-2 tiles from a shared counter in reverse order, so
 // that the first tiles packed are the ones pass 1 read last, still in L2, and
 // no CTA waits at the end on a fixed share of slow (fallback-heavy) tiles.
+// `extra_arrivals` (0 in every product call) raises the barrier's arrival
+// target above the grid size and `wait_ns` sets its limit: the
+// failure-detection entry point uses them to make the wait give up.
 // ---------------------------------------------------------------------------
 constexpr uint64_t kGridWaitLimitNs = 2000000000ull;
 constexpr uint32_t ERR_GRID_WAIT = 1u << 8;   // the cooperative producer's grid barrier timed out
@@ -595,7 +598,7 @@ template <class Src1, class Src2>
 __global__ void __launch_bounds__(kThreads, min_blocks<Src1>())
     producer_coop_kernel(Src1 src1, Src2 src2, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
                          int64_t n_tiles1, int64_t n_tiles2, uint32_t *scratch, float *ts_out, uint8_t *qdata,
-                         uint8_t *sf)
+                         uint8_t *sf, uint32_t extra_arrivals, uint64_t wait_ns)
 {
     __shared__ __align__(16) uint8_t sft[4 * 512];
     __shared__ float ts_sh;
@@ -612,9 +615,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks<Src1>())
         while (true) {
             uint32_t arrived;
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(arrived) : "l"(scratch + 1) : "memory");
-            if (arrived >= gridDim.x)
+            if (arrived >= gridDim.x + extra_arrivals)
                 break;
-            if (globaltimer_ns() - t0 > kGridWaitLimitNs) {
+            if (globaltimer_ns() - t0 > wait_ns) {
                 ok = false;
                 atomicOr(&g_producer_error, ERR_GRID_WAIT);
                 break;
@@ -687,7 +690,8 @@ cudaError_t run_absmax(const Src &src, int64_t m, int64_t d, float *ts, uint32_t
 // grid barrier cannot wait on a CTA that is not running.
 template <class Src1, class Src2>
 cudaError_t run_coop(const Src1 &src1, const Src2 &src2, int64_t m, int64_t m_pad, int64_t d, float *ts,
-                     uint32_t *scratch, uint8_t *qdata, uint8_t *sf, cudaStream_t st)
+                     uint32_t *scratch, uint8_t *qdata, uint8_t *sf, cudaStream_t st, uint32_t extra_arrivals = 0,
+                     uint64_t wait_ns = kGridWaitLimitNs)
 {
     const int col_tiles = static_cast<int>(d / kTileCols);
     const int64_t n_tiles1 = ((m + kTileRows - 1) / kTileRows) * col_tiles;
@@ -710,7 +714,7 @@ cudaError_t run_coop(const Src1 &src1, const Src2 &src2, int64_t m, int64_t m_pa
         return cudaErrorInvalidValue;
     void *args[] = {const_cast<Src1 *>(&src1), const_cast<Src2 *>(&src2), &m, &m_pad, &d,
                     const_cast<int *>(&col_tiles), const_cast<int64_t *>(&n_tiles1), const_cast<int64_t *>(&n_tiles2),
-                    &scratch, &ts, &qdata, &sf};
+                    &scratch, &ts, &qdata, &sf, &extra_arrivals, &wait_ns};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(producer_coop_kernel<Src1, Src2>), dim3(grid),
                                        dim3(kThreads), args, 0, st);
 }
@@ -769,6 +773,14 @@ cudaError_t launch_quantize_pack(const uint16_t *x, int64_t ldx, int64_t m, int6
 {
     PlainSrc src{x, ldx};
     return run_coop(src, src, m, m_pad, d, ts, scratch, qdata, sf, st);
+}
+
+cudaError_t launch_quantize_pack_barrier_timeout(const uint16_t *x, int64_t ldx, int64_t m, int64_t m_pad,
+                                                int64_t d, float *ts, uint32_t *scratch, uint8_t *qdata, uint8_t *sf,
+                                                uint64_t wait_ns, cudaStream_t st)
+{
+    PlainSrc src{x, ldx};
+    return run_coop(src, src, m, m_pad, d, ts, scratch, qdata, sf, st, 1u, wait_ns);
 }
 
 cudaError_t launch_modulate_produce(const uint16_t *x, int64_t ldx, int64_t m, int64_t m_pad, int64_t d,

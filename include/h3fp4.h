@@ -279,7 +279,9 @@ H3FP4_API h3fp4_status h3fp4_swizzle_scales(const uint8_t *sf_logical, int64_t r
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and may load the library's device code; make that first
- * call before any stream capture.  All calls share the array and it keeps the
+ * call before any stream capture.  The address is kept for the life of the
+ * process's context on that device: after cudaDeviceReset, do not call this
+ * entry point again in that process.  All calls share the array and it keeps the
  * last call's contents (each call clears its counters and rewrites h before
  * reading it); calls whose GPU work overlaps race on it and must be
  * serialised by the caller.
@@ -293,10 +295,45 @@ H3FP4_API h3fp4_status h3fp4_swiglu_pack_noalloc(const void *gate_bf16, int64_t 
 /*
  * h3fp4_device_error -- reads and clears the device-side error word of the
  * current device (synchronous).  Kernels whose pipeline waits give up after
- * their time limit record a nonzero code there instead of hanging.
+ * their time limit (2 s) record a nonzero code there instead of hanging, and
+ * return.  Bits: GEMM waits 1 (a free stage), 2 (operands landed), 4 (a
+ * finished accumulator), 8 (a drained accumulator), 16 (scale atoms landed);
+ * 256 the cooperative producer's grid barrier.
  * Returns H3FP4_OK and stores the word in *code (0 = no error).
  */
 H3FP4_API h3fp4_status h3fp4_device_error(uint32_t *code);
+
+/*
+ * Failure detection -- diagnostics, not part of the hot path.  No counterpart
+ * on the source pages beyond the bounded waits themselves ("NVFP4 Streaming
+ * Design", P2: a cooperative producer around a grid barrier with a bounded
+ * wait).  Each call runs one of the library's kernels with a wait that cannot
+ * be satisfied and a limit of limit_us microseconds (1 .. 2,000,000, else
+ * H3FP4_ERR_SHAPE), so that a caller can check that a wait which runs out
+ * ends the kernel with an error code instead of a hang, and that the device
+ * stays usable afterwards.
+ *
+ * h3fp4_diag_producer_barrier_timeout -- the cooperative plain producer
+ * (h3fp4_quantize_pack's kernel, same arguments and checks) with its grid
+ * barrier's arrival target one above the grid size: every CTA gives up after
+ * limit_us, records bit 256 and returns.  tensor_scale, qdata and sfa are not
+ * written; pass 1 reads x.
+ *
+ * h3fp4_diag_gemm_wait_timeout -- the default GEMM kernel (same arguments
+ * and checks as h3fp4_gemm, default configuration) with its operand loads
+ * withheld: the scale-copy, MMA and epilogue warps' waits run out after
+ * limit_us and record bits 16, 2 and 4.  c_bf16 is not written and no
+ * operand is read.
+ */
+H3FP4_API h3fp4_status h3fp4_diag_producer_barrier_timeout(const void *x_bf16, int64_t ldx, int64_t m,
+                                                           int64_t m_pad, int64_t d, float *tensor_scale,
+                                                           uint32_t *scratch, uint8_t *qdata, uint8_t *sfa,
+                                                           uint32_t limit_us, void *stream);
+H3FP4_API h3fp4_status h3fp4_diag_gemm_wait_timeout(const uint8_t *a_q, const uint8_t *a_sf,
+                                                    const float *a_tensor_scale, const uint8_t *b_q,
+                                                    const uint8_t *b_sf, const float *b_tensor_scale, void *c_bf16,
+                                                    int64_t ldc, int64_t m, int64_t m_pad, int64_t n, int64_t k,
+                                                    uint32_t limit_us, void *stream);
 
 /* Human-readable name of a status code (static string). */
 H3FP4_API const char *h3fp4_status_string(h3fp4_status status);

@@ -171,6 +171,18 @@ def test_gemm_gated_residual_validation(L):
     assert call(cfg=ctypes.byref(pkg.GemmConfig(0, 0, 3, 0))) == UNSUP     # no such kernel
 
 
+def test_failure_detection_entry_points_validation(L):
+    f = L.h3fp4_diag_producer_barrier_timeout
+    assert f(None, 256, 10, 16, 256, F, F, F, F, 1000, None) == NULL
+    assert f(F, 256, 10, 16, 256, F, F, F, F, 0, None) == SHAPE              # limit must be >= 1 us
+    assert f(F, 256, 10, 16, 256, F, F, F, F, 2000001, None) == SHAPE        # and <= 2 s
+    assert f(F, 256, 10, 20, 256, F, F, F, F, 1000, None) == SHAPE           # m_pad not a multiple of 16
+    g = L.h3fp4_diag_gemm_wait_timeout
+    assert g(F, F, F, F, F, F, None, 384, 300, 320, 384, 256, 1000, None) == NULL
+    assert g(F, F, F, F, F, F, F, 384, 300, 320, 384, 128, 1000, None) == SHAPE     # k not a multiple of 256
+    assert g(F, F, F, F, F, F, F, 384, 300, 320, 384, 256, 0, None) == SHAPE
+
+
 def test_swizzle_and_device_error_validation(L):
     assert L.h3fp4_swizzle_scales(None, 10, 16, 16, F, None) == NULL
     assert L.h3fp4_swizzle_scales(F, 10, 6, 16, F, None) == SHAPE

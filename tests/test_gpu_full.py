@@ -1,12 +1,20 @@
 """Full-size parity at the 37,810-token workloads, in the launch configuration
-the benchmark times: the benchmark's three linears and the model's own four
-projection widths.
+the benchmark times: the producer-only workload, the benchmark's three linears
+and the model's own four projection widths.
 
-The oracle recomputes the global tensor scale over the whole activation (a
-plain pass in C), packs a sample of rows (the first and last rows of tiles,
-the last logical rows and random rows) and evaluates those rows of the GEMM
-over every output column; the GPU results must match bit for bit (producer)
-and within the GEMM tolerance.  The padding rows must be zero.
+Producer: the oracle recomputes every row (modulation or SwiGLU, the global
+absolute maximum, the tensor scale, the E4M3 block scales and E2M1 codes of
+all 37,810 rows, and the zero padding up to the scale layout's 128-row
+multiple); the GPU's tensor scale, QDATA and scale buffer must equal it byte
+for byte, every row and every padding byte included ("NVFP4 Modulation
+Producer Fusion", Exactness Contract and Result: byte-identical QDATA and E4M3
+block scales for complete 37,810-row inputs).
+
+GEMM: whole 256-row output tiles of the default kernel -- the first, the last
+(partial: 178 rows) and the two on either side of the segment boundary at row
+32,768 -- plus random rows, over every output column, against the oracle's
+FP64 sums of its own packed rows (never the GPU's bytes); each output within
+1 bf16 ulp + 1e-5 * sum |a_k b_k|.
 """
 import numpy as np
 import pytest
@@ -17,84 +25,41 @@ from dit_modulate_absmax_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-
-def _sample_rows(m, seed):
-    rng = np.random.default_rng(seed)
-    fixed = [0, 1, 127, 128, 255, 32767, 32768, m - 129, m - 128, m - 2, m - 1]
-    return np.unique(np.concatenate([fixed, rng.integers(0, m, size=13)]))
+PAIR_TILE_M = 256
 
 
-def _check_producer_rows(w, rows, y_rows, ts_o, q_gpu, sf_gpu):
-    """Pack the sampled rows with the oracle and compare their bytes."""
-    q_o, sf_o = oracle.pack(y_rows, len(rows), ts_o)
-    nb = w.k // 16
-    sf_logical = oracle.unswizzle_sf(sf_gpu, -(-w.m_pad // 128) * 128, nb)
-    assert np.array_equal(q_gpu[rows], q_o[: len(rows)])
-    assert np.array_equal(sf_logical[rows], sf_o[: len(rows)])
-    assert not q_gpu[w.m:].any(), "padding rows of QDATA must be zero"
-    assert not sf_logical[w.m:].any(), "scales of rows >= m must be zero"
-    return q_o[: len(rows)], sf_o
+def _gemm_rows(m, seed):
+    """Rows of whole M tiles (first, last, both sides of row 32,768) plus random rows."""
+    last = (m - 1) // PAIR_TILE_M
+    tiles = sorted({0, last, 32_768 // PAIR_TILE_M - 1, 32_768 // PAIR_TILE_M})
+    rows = [np.arange(t * PAIR_TILE_M, min(m, (t + 1) * PAIR_TILE_M)) for t in tiles]
+    rows.append(np.random.default_rng(seed).integers(0, m, size=16))
+    return np.unique(np.concatenate(rows))
 
 
-def _check_gemm_rows(w, rows, q_o, sf_o, ts_o, wt, C):
-    """GEMM rows `rows` against the oracle's own packed rows (never the GPU's bytes)."""
-    R, S = oracle.gemm_reference(q_o, sf_o, ts_o, wt["q"].cpu().numpy(), wt["sf"].cpu().numpy(), wt["ts"],
-                                 w.k, rows=np.arange(len(rows)))
-    ok, err, tol = oracle.gemm_check(C[rows], R, S)
-    assert ok.all(), f"{int((~ok).sum())} outputs outside tolerance (max err/tol {float((err / tol).max()):.3g})"
-    return float((err / tol).max())
+def _u16(t):
+    return t.cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("name", ["qkv", "fc1"])
-def test_modulate_linear_full_size(h3, name):
-    w = W.WORKLOADS[name]
-    dev = torch.device("cuda")
-    act = W.activations(w, device=dev)
-    off = W.seg_offsets(w)
-    wt = W.weights(w, device=dev)
-    ts = h3.modulate_absmax(act["x"], act["shift"], act["scale"], off)
-    q, sfa = h3.modulate_pack(act["x"], act["shift"], act["scale"], off, ts, w.m_pad)
-    bsf = h3.swizzle_scales(wt["sf"][: w.n])
-    bts = torch.tensor([wt["ts"]], dtype=torch.float32, device=dev)
-    C = h3.gemm(q, sfa, ts, wt["q"], bsf, bts, w.m)
-    torch.cuda.synchronize()
-    assert h3.h3fp4_device_error() == 0
-
-    x = act["x"].cpu().numpy().view(np.uint16)
-    sh = act["shift"].cpu().numpy().view(np.uint16)
-    sc = act["scale"].cpu().numpy().view(np.uint16)
-    y = oracle.modulate(x, sh, sc, off)
+def _check_producer_all_rows(w, y, ts, q, sfa):
+    """Every byte of the GPU's producer outputs against the oracle's pack of all rows of y."""
     ts_o = oracle.tensor_scale(oracle.absmax(y))
-    assert float(ts.item()) == ts_o
-    rows = _sample_rows(w.m, seed=31)
-    q_o, sf_o = _check_producer_rows(w, rows, y[rows], ts_o, q.cpu().numpy(), sfa.cpu().numpy())
-    _check_gemm_rows(w, rows, q_o, sf_o, ts_o, wt, C.cpu().numpy().view(np.uint16))
+    got_ts = np.float32(ts.item())
+    assert got_ts.view(np.uint32) == np.float32(ts_o).view(np.uint32), (float(got_ts), ts_o)
+    q_o, sf_o = oracle.pack(y, w.m_pad, ts_o)
+    q_g = q.cpu().numpy()
+    bad = np.flatnonzero((q_g != q_o).any(axis=1))
+    assert bad.size == 0, f"QDATA differs in {bad.size} of {w.m_pad} rows (first {bad[:5].tolist()})"
+    sfa_g = sfa.cpu().numpy()
+    sf_g = oracle.unswizzle_sf(sfa_g, sf_o.shape[0], sf_o.shape[1])
+    bad = np.flatnonzero((sf_g != sf_o).any(axis=1))
+    assert bad.size == 0, f"block scales differ in {bad.size} rows (first {bad[:5].tolist()})"
+    assert np.array_equal(sfa_g, oracle.swizzle_sf(sf_o)), "scale buffer differs from the oracle's layout"
+    assert not q_o[w.m:].any() and not sf_o[w.m:].any()   # the oracle's own padding reading
+    return ts_o, q_o, sf_o
 
 
-def test_swiglu_linear_full_size(h3):
-    w = W.WORKLOADS["fc2"]
-    dev = torch.device("cuda")
-    act = W.activations(w, device=dev)
-    wt = W.weights(w, device=dev)
-    ts, q, sfa = h3.swiglu_pack(act["gate"], act["up"], w.m_pad)
-    bsf = h3.swizzle_scales(wt["sf"][: w.n])
-    bts = torch.tensor([wt["ts"]], dtype=torch.float32, device=dev)
-    C = h3.gemm(q, sfa, ts, wt["q"], bsf, bts, w.m)
-    torch.cuda.synchronize()
-    assert h3.h3fp4_device_error() == 0
-
-    h = oracle.swiglu(act["gate"].cpu().numpy().view(np.uint16), act["up"].cpu().numpy().view(np.uint16))
-    ts_o = oracle.tensor_scale(oracle.absmax(h))
-    assert float(ts.item()) == ts_o
-    rows = _sample_rows(w.m, seed=32)
-    q_o, sf_o = _check_producer_rows(w, rows, h[rows], ts_o, q.cpu().numpy(), sfa.cpu().numpy())
-    _check_gemm_rows(w, rows, q_o, sf_o, ts_o, wt, C.cpu().numpy().view(np.uint16))
-
-
-# ---------------------------------------------------------------------------
-# The model's own projection widths (hidden 5,376, attention 7,168, MLP 14,336)
-# ---------------------------------------------------------------------------
-def _weights_and_gemm(h3, w, q, sfa, ts, dev):
+def _gemm(h3, w, q, sfa, ts, dev):
     wt = W.weights(w, device=dev)
     bsf = h3.swizzle_scales(wt["sf"][: w.n])
     bts = torch.tensor([wt["ts"]], dtype=torch.float32, device=dev)
@@ -104,22 +69,63 @@ def _weights_and_gemm(h3, w, q, sfa, ts, dev):
     return wt, C
 
 
-@pytest.mark.parametrize("name", ["h3_qkv", "h3_fc1"])
-def test_model_width_modulate_linear(h3, name):
+def _check_gemm_rows(w, q_o, sf_o, ts_o, wt, C, seed):
+    rows = _gemm_rows(w.m, seed)
+    R, S = oracle.gemm_reference(q_o, sf_o, ts_o, wt["q"].cpu().numpy(), wt["sf"].cpu().numpy(), wt["ts"], w.k,
+                                 rows=rows)
+    got = _u16(C[torch.from_numpy(rows).to(C.device)])
+    ok, err, tol = oracle.gemm_check(got, R, S)
+    assert ok.all(), f"{int((~ok).sum())} outputs outside tolerance (max err/tol {float((err / tol).max()):.3g})"
+
+
+def _modulate_y(act, off):
+    return oracle.modulate(_u16(act["x"]), _u16(act["shift"]), _u16(act["scale"]), off)
+
+
+def test_producer_workload_full_size_both_launch_forms(h3):
+    """The producer-only configuration (37,810 x 7,168, two segments), through
+    the two-launch form (h3fp4_modulate_absmax + h3fp4_modulate_pack) and the
+    single cooperative launch (h3fp4_modulate_produce)."""
+    w = W.WORKLOADS["producer"]
+    dev = torch.device("cuda")
+    act = W.activations(w, device=dev)
+    off = W.seg_offsets(w)
+    ts = h3.modulate_absmax(act["x"], act["shift"], act["scale"], off)
+    q, sfa = h3.modulate_pack(act["x"], act["shift"], act["scale"], off, ts, w.m_pad)
+    ts1, q1, sfa1 = h3.modulate_produce(act["x"], act["shift"], act["scale"], off, w.m_pad)
+    torch.cuda.synchronize()
+    assert h3.h3fp4_device_error() == 0
+    y = _modulate_y(act, off)
+    _check_producer_all_rows(w, y, ts, q, sfa)
+    _check_producer_all_rows(w, y, ts1, q1, sfa1)
+
+
+@pytest.mark.parametrize("name", ["qkv", "fc1", "h3_qkv", "h3_fc1"])
+def test_modulate_linear_full_size(h3, name):
     w = W.WORKLOADS[name]
     dev = torch.device("cuda")
     act = W.activations(w, device=dev)
     off = W.seg_offsets(w)
     ts = h3.modulate_absmax(act["x"], act["shift"], act["scale"], off)
     q, sfa = h3.modulate_pack(act["x"], act["shift"], act["scale"], off, ts, w.m_pad)
-    wt, C = _weights_and_gemm(h3, w, q, sfa, ts, dev)
-    y = oracle.modulate(act["x"].cpu().numpy().view(np.uint16), act["shift"].cpu().numpy().view(np.uint16),
-                        act["scale"].cpu().numpy().view(np.uint16), off)
-    ts_o = oracle.tensor_scale(oracle.absmax(y))
-    assert float(ts.item()) == ts_o
-    rows = _sample_rows(w.m, seed=33)
-    q_o, sf_o = _check_producer_rows(w, rows, y[rows], ts_o, q.cpu().numpy(), sfa.cpu().numpy())
-    _check_gemm_rows(w, rows, q_o, sf_o, ts_o, wt, C.cpu().numpy().view(np.uint16))
+    wt, C = _gemm(h3, w, q, sfa, ts, dev)
+    ts_o, q_o, sf_o = _check_producer_all_rows(w, _modulate_y(act, off), ts, q, sfa)
+    _check_gemm_rows(w, q_o, sf_o, ts_o, wt, C, seed=31)
+
+
+@pytest.mark.parametrize("name,workspace", [("fc2", False), ("h3_fc2", True)])
+def test_swiglu_linear_full_size(h3, name, workspace):
+    w = W.WORKLOADS[name]
+    dev = torch.device("cuda")
+    act = W.activations(w, device=dev)
+    hw = torch.empty(w.m, w.k, dtype=torch.int16, device=dev) if workspace else None
+    ts, q, sfa = h3.swiglu_pack(act["gate"], act["up"], w.m_pad, h_workspace=hw)
+    wt, C = _gemm(h3, w, q, sfa, ts, dev)
+    h = oracle.swiglu(_u16(act["gate"]), _u16(act["up"]))
+    if workspace:
+        assert np.array_equal(_u16(hw), h), "materialised h differs from the oracle"
+    ts_o, q_o, sf_o = _check_producer_all_rows(w, h, ts, q, sfa)
+    _check_gemm_rows(w, q_o, sf_o, ts_o, wt, C, seed=32)
 
 
 def test_model_width_attention_output_linear(h3):
@@ -127,26 +133,6 @@ def test_model_width_attention_output_linear(h3):
     dev = torch.device("cuda")
     act = W.activations(w, device=dev)
     ts, q, sfa = h3.quantize_pack(act["x"], w.m_pad)
-    wt, C = _weights_and_gemm(h3, w, q, sfa, ts, dev)
-    x = act["x"].cpu().numpy().view(np.uint16)
-    ts_o = oracle.tensor_scale(oracle.absmax(x))
-    assert float(ts.item()) == ts_o
-    rows = _sample_rows(w.m, seed=34)
-    q_o, sf_o = _check_producer_rows(w, rows, x[rows], ts_o, q.cpu().numpy(), sfa.cpu().numpy())
-    _check_gemm_rows(w, rows, q_o, sf_o, ts_o, wt, C.cpu().numpy().view(np.uint16))
-
-
-def test_model_width_swiglu_linear(h3):
-    w = W.WORKLOADS["h3_fc2"]
-    dev = torch.device("cuda")
-    act = W.activations(w, device=dev)
-    hw = torch.empty(w.m, w.k, dtype=torch.int16, device=dev)
-    ts, q, sfa = h3.swiglu_pack(act["gate"], act["up"], w.m_pad, h_workspace=hw)
-    wt, C = _weights_and_gemm(h3, w, q, sfa, ts, dev)
-    h = oracle.swiglu(act["gate"].cpu().numpy().view(np.uint16), act["up"].cpu().numpy().view(np.uint16))
-    ts_o = oracle.tensor_scale(oracle.absmax(h))
-    assert float(ts.item()) == ts_o
-    assert np.array_equal(hw.cpu().numpy().view(np.uint16), h)
-    rows = _sample_rows(w.m, seed=35)
-    q_o, sf_o = _check_producer_rows(w, rows, h[rows], ts_o, q.cpu().numpy(), sfa.cpu().numpy())
-    _check_gemm_rows(w, rows, q_o, sf_o, ts_o, wt, C.cpu().numpy().view(np.uint16))
+    wt, C = _gemm(h3, w, q, sfa, ts, dev)
+    ts_o, q_o, sf_o = _check_producer_all_rows(w, _u16(act["x"]), ts, q, sfa)
+    _check_gemm_rows(w, q_o, sf_o, ts_o, wt, C, seed=34)

@@ -404,6 +404,63 @@ def test_gated_residual_matches_torch_bf16_ops():
     assert np.array_equal(out, bits(res + gsel * c))
 
 
+def _all_finite_bf16():
+    """Every finite bf16 value, sorted (from the 2^16 patterns through torch's bf16 view)."""
+    pats = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).double().numpy()
+    return np.unique(pats[np.isfinite(pats)])
+
+
+def test_bf16_directed_rounding_matches_brute_force():
+    """_bf16_directed(v, up) is the smallest bf16 >= v (up) or the largest <= v,
+    found here by binary search over the sorted list of every finite bf16."""
+    allv = _all_finite_bf16()
+    rng = np.random.default_rng(47)
+    v = np.concatenate([
+        rng.standard_normal(2000) * 10.0 ** rng.integers(-40, 38, size=2000),
+        allv[rng.integers(0, allv.size, size=500)],                       # exact bf16 values
+        (allv[1000:1500] + allv[1001:1501]) / 2,                          # exact midpoints
+        [0.0, -0.0, 1e-45, -1e-45, 2.0 ** -133, -(2.0 ** -133), 2.0 ** -126, 3.0e38, -3.0e38],
+    ])
+    v = v[np.abs(v) <= allv[-1]]
+    up = oracle.bf16_to_f64(oracle._bf16_directed(v, up=True))
+    down = oracle.bf16_to_f64(oracle._bf16_directed(v, up=False))
+    want_up = allv[np.searchsorted(allv, v, side="left")]
+    want_down = allv[np.searchsorted(allv, v, side="right") - 1]
+    assert np.array_equal(up, want_up)
+    assert np.array_equal(down, want_down)
+
+
+def test_gated_residual_bounds_match_brute_force_over_the_tolerance_interval():
+    """gated_residual_bounds(R, S, ...) returns the smallest and largest output of
+    the gated epilogue over every bf16 value c within the GEMM tolerance of R:
+    enumerate those c one by one and evaluate RN(res + RN(gate_s * c)) with
+    torch's CPU bf16 ops (an independent evaluator), then compare."""
+    allv = _all_finite_bf16()
+    rng = np.random.default_rng(53)
+    m, n = 6, 24
+    R = rng.standard_normal((m, n)) * 4.0
+    R[0, :4] = [0.0, 1e-3, -1e-3, 5e-39]                  # intervals that contain or reach 0
+    S = np.abs(R) * rng.uniform(1.0, 400.0, size=(m, n)) + 1e-3
+    gate_t = torch.randn(2, n, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    gate_t[1, :6] = torch.tensor([-2.0, -0.5, 0.0, -0.0, 3.0, -1e-3])  # negative gates: decreasing maps
+    res_t = (torch.randn(m, n, generator=torch.Generator().manual_seed(4)) * 8).to(torch.bfloat16)
+    off = [0, 3, m]
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    lo, hi = oracle.gated_residual_bounds(R, S, bits(gate_t), off, bits(res_t))
+    tol = oracle.gemm_tolerance(R, S)
+    counted = 0
+    for i in range(m):
+        g = gate_t[0 if i < 3 else 1]
+        for j in range(n):
+            cs = allv[(allv >= R[i, j] - tol[i, j]) & (allv <= R[i, j] + tol[i, j])]
+            assert cs.size >= 1
+            counted += cs.size
+            c = torch.tensor(cs, dtype=torch.float64).to(torch.bfloat16)
+            outs = (res_t[i, j] + g[j] * c).double().numpy()
+            assert lo[i, j] == outs.min() and hi[i, j] == outs.max(), (i, j, cs.size)
+    assert counted > 10 * m * n   # the intervals hold many candidates, not just R's neighbours
+
+
 # ---------------------------------------------------------------------------
 # GEMM reference
 # ---------------------------------------------------------------------------
