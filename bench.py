@@ -432,6 +432,21 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     assert h3.h3fp4_device_error() == 0
 
+    # Each producer alone, back to back (10 runs, median): in the step it follows
+    # the previous linear's GEMM, whose ~100 MB of dirty output lines in L2 are
+    # written back while pass 1 streams its input; alone, the producer's HBM
+    # traffic is its own.
+    standalone = {}
+    for L in lins:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(11)]
+        for e0, e1 in evs:
+            e0.record()
+            L.produce()
+            e1.record()
+        torch.cuda.synchronize()
+        standalone[L.name] = _pct([e0.elapsed_time(e1) for e0, e1 in evs[1:]], 0.5)
+    assert h3.h3fp4_device_error() == 0
+
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in lins] for _ in range(args.steps)]
 
     def timed_steps():
@@ -559,6 +574,8 @@ def run_ours(args, rank, world, local_rank):
             "producer_hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
             "producer_hbm_frac_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
             "producer_ms_p50_p95": [round(v, 4) for v in p["producer_p50_p95"]],
+            "producer_ms_standalone": round(standalone[L.name], 4),
+            "producer_hbm_frac_standalone": round(L.prod_bytes / (standalone[L.name] * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "gemm_ms": round(p["gemm_ms"], 4), "gemm_tflops": round(tfl, 1),
             "gemm_ms_p50_p95": [round(v, 4) for v in p["gemm_p50_p95"]],
             "epilogue": "gated residual" if L.gated else "bf16",
