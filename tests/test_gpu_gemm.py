@@ -85,6 +85,31 @@ def test_exact_products_are_bit_exact(h3, cfg):
     assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:4].tolist()}"
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+@pytest.mark.parametrize("n_group", [1, 2, 3, 5])
+def test_tile_schedules_are_bit_exact(h3, kernel, n_group):
+    """Every N-group size visits every output tile once: groups of n_group N-tiles
+    sweep M forwards and backwards in turn (a ragged last group included), with
+    5 M-tiles (the last partial) and 5 N-tiles of 256 columns.  Power-of-two
+    scales keep every sum exact, so C = RN_bf16(R) bit for bit."""
+    rng = np.random.default_rng(30 + n_group)
+    m, m_pad, n, k = 1100, 1104, 1280, 512
+    pow2 = np.array([0x28, 0x30, 0x38], dtype=np.uint8)
+    qa = rng.integers(0, 256, size=(m_pad, k // 2), dtype=np.uint8)
+    qa[m:] = 0
+    qb = rng.integers(0, 256, size=(n, k // 2), dtype=np.uint8)
+    sfa = np.zeros((h3.sf_rows(m_pad), k // 16), dtype=np.uint8)
+    sfb = np.zeros((n, k // 16), dtype=np.uint8)
+    sfa[:m] = rng.choice(pow2, size=(m, k // 16))
+    sfb[:] = rng.choice(pow2, size=(n, k // 16))
+    cfg = h3.GemmConfig(n_group, 0, KERNELS[kernel], 0)
+    C = run_gemm(h3, qa, sfa, 0.5, qb, sfb, 0.25, m, cfg=cfg)
+    R, _ = oracle.gemm_reference(qa, sfa, 0.5, qb, sfb, 0.25, k, rows=np.arange(m))
+    want = np.vectorize(oracle.bf16_bits)(R).astype(np.uint16)
+    bad = np.argwhere(C != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:4].tolist()}"
+
+
 @pytest.mark.parametrize("m,m_pad,n,k", [
     (1, 16, 128, 256),
     (130, 144, 256, 768),
