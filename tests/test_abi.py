@@ -40,6 +40,21 @@ def test_library_exports_every_declared_symbol(L):
     assert set(_declared()) <= exported
 
 
+def test_header_is_plain_c_and_the_library_links_from_c(L, tmp_path):
+    """A C11 program (gcc, -Wall -Werror -pedantic) includes the header, links
+    libh3fp4.so directly and calls entry points that need no GPU."""
+    exe = tmp_path / "abi_c_check"
+    src = os.path.join(ROOT, "tests", "helpers", "abi_c_check.c")
+    libdir = os.path.dirname(pkg.LIB_PATH)
+    cmd = ["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+           src, "-o", str(exe), f"-L{libdir}", "-l:libh3fp4.so", f"-Wl,-rpath,{libdir}"]
+    import subprocess
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
 def test_status_strings_and_build_info(L):
     assert pkg.lib().h3fp4_status_string(0) == b"ok"
     assert pkg.lib().h3fp4_status_string(3) == b"invalid shape"
