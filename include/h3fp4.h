@@ -12,6 +12,11 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Every call only enqueues work on that stream and returns; nothing
  *    synchronises the host.  Outputs are valid once the stream reaches them.
+ *    The first call of an entry point on a device sets its kernels'
+ *    attributes; after that, h3fp4_modulate_absmax, h3fp4_modulate_pack,
+ *    h3fp4_swiglu_pack and h3fp4_gemm may be captured into a CUDA graph and
+ *    replayed (the captured calls keep their pointers; new inputs are copied
+ *    into the same buffers).
  *  - Arguments are checked on the host before anything is enqueued.  A failed
  *    check returns an error status and enqueues nothing.  A CUDA launch error
  *    returns H3FP4_ERR_CUDA (the CUDA error itself stays readable with
