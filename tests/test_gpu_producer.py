@@ -139,6 +139,24 @@ def test_small_amax_tensor(h3):
     check_modulate(h3, x, sh, sc, [0, m], 64)
 
 
+@pytest.mark.parametrize("log2_amax", [-60, -78, -79, -80, -81, -84, 100, 107, 108, 109, 110, 127])
+def test_tensor_scales_at_the_edges_of_the_division_free_range(h3, log2_amax):
+    """The pack divides without a division instruction while 6 ts lies in
+    [2^-88, 2^100] and a block's scale product in [2^-100, 2^100], and by the
+    IEEE division outside; tensors whose absolute maximum puts 6 ts on either
+    side of those limits, with rows spanning 30 binades (so that block scale
+    products fall on both sides too), must still match the oracle bit for bit."""
+    m, d = 120, 512
+    g = torch.Generator().manual_seed(40 + log2_amax)
+    rows = torch.pow(2.0, -0.25 * torch.arange(m, dtype=torch.float64)).unsqueeze(1)
+    v = torch.randn(m, d, generator=g, dtype=torch.float64) * rows
+    v = v / v.abs().max() * 2.0 ** log2_amax
+    x = _bf16(v.float())
+    sh = np.zeros((1, d), dtype=np.uint16)
+    sc = _bf16(torch.randn(1, d, generator=g) * 0.01)
+    check_modulate(h3, x, sh, sc, [0, m], 128)
+
+
 def test_zero_rows_gives_zero_scale(h3):
     d, m_pad = 256, 32
     x = np.zeros((0, d), dtype=np.uint16)
