@@ -446,7 +446,8 @@ __device__ __forceinline__ float2 div2_rn_by_rcp(float2 a, float2 b, float2 rb)
 // comes from rden = RN(1/den) by the residual correction; block maxima below
 // 2^-100 then give quotients below 2^-12, whose code is 0 however they round.
 // Other dens (tensors whose absolute maximum is below ~2^-80 or above ~2^108,
-// or zero) take the IEEE division.
+// zero, or not finite) take the IEEE division.  A block maximum is NaN when
+// the block holds a NaN (absmax16), and then so is the tensor scale.
 __device__ __forceinline__ uint32_t block_scale(uint32_t bmax_bits, float den, float rden, bool den_fma)
 {
     const float b = __uint_as_float(bmax_bits << 16);
@@ -454,12 +455,13 @@ __device__ __forceinline__ uint32_t block_scale(uint32_t bmax_bits, float den, f
         return cvt_e4m3(div_rn_by_rcp(b, den, rden));
     if (bmax_bits == 0)
         return 0u;  // an all-zero block gets scale 0
-    return cvt_e4m3(__fdiv_rn(b, den));
+    const float q = __fdiv_rn(b, den);
+    return q != q ? 0x7Fu : cvt_e4m3(q);   // a NaN quotient (NaN or infinite ts) is the E4M3 NaN code
 }
 
 // E2M1 codes of a 16-value block with the block's FP32 scale product sc;
-// byte i holds element 2i in its low nibble.  A zero scale product gives
-// signed zeros.
+// byte i holds element 2i in its low nibble.  A zero or NaN scale product
+// (sc is never negative) gives zeros with y's signs.
 //
 // The code of y is E2M1_RNE_sat(RN_f32(y / sc)).  For sc in [2^-100, 2^100]
 // the quotients come from r = RN(1/sc) (one correctly rounded reciprocal per
@@ -471,7 +473,7 @@ __device__ __forceinline__ uint32_t block_scale(uint32_t bmax_bits, float den, f
 // y = -0) carries through into the code.
 __device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
 {
-    if (sc == 0.0f) {
+    if (!(sc > 0.0f)) {
         uint32_t signs[2] = {0u, 0u};
 #pragma unroll
         for (int i = 0; i < 8; ++i)

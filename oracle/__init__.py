@@ -31,8 +31,10 @@ rounding routine); sums of products use numpy FP64 matmul as a library step.
 Parity pins: every function above is pinned by ``tests/test_oracle_pins.py``
 against brute force, closed forms, a library routine (torch CPU BF16 ops,
 torch float8_e4m3fn casts) or hand-derived golden values in ``tests/golden``.
-Parity unpinned: the NaN/Inf input behaviour of the pack (the pages list such
-inputs as adversarial cases but give no expected bytes).
+NaN/Inf inputs (adversarial cases the pages list without expected bytes)
+follow the formulas in IEEE arithmetic with two stated conventions -- a NaN
+quotient encodes as the E4M3 NaN code 0x7F, and a zero or NaN scale product
+gives zeros with y's signs -- pinned by hand-derived bytes.
 """
 from __future__ import annotations
 

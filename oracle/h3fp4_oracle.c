@@ -281,6 +281,12 @@ float orc_tensor_scale(uint16_t amax_bits)
 
 /* ---------------------------------------------------------------------------
  * NVFP4 pack, "NVFP4 Streaming Design", Numerical Constraint items 3-4.
+ * Non-finite inputs (listed as adversarial cases in the Validation Ladder,
+ * item 1, with no expected bytes) follow the same formulas in IEEE
+ * arithmetic: a NaN in a block makes its maximum NaN, a NaN quotient encodes
+ * as the E4M3 NaN code 0x7F (a tensor scale that is NaN, from a NaN anywhere,
+ * or infinite, from an infinity, gives such quotients), and a block whose
+ * scale product is zero or NaN gets zeros with y's signs.
  * y is [m, d] bf16 (logical rows).  Writes
  *   qdata [m_pad, d/2]: byte (r, j/2) = code(r, j) | code(r, j+1) << 4,
  *   sf    [sf_rows, d/16] (LOGICAL row-major, not swizzled): E4M3 codes,
@@ -300,11 +306,13 @@ void orc_pack(const uint16_t *y, int64_t ldy, int64_t m, int64_t m_pad, int64_t 
             double v[16], bamax = 0.0;
             for (int j = 0; j < 16; ++j) {
                 v[j] = orc_bf16_value(y[r * ldy + b * 16 + j]);
-                if (fabs(v[j]) > bamax)
+                if (v[j] != v[j])
+                    bamax = NAN;                    /* a NaN makes the block maximum NaN */
+                else if (fabs(v[j]) > bamax)
                     bamax = fabs(v[j]);
             }
-            uint8_t bs = 0;
-            if (bamax != 0.0)
+            uint8_t bs = 0;                         /* an all-zero block gets scale 0 */
+            if (bamax != 0.0)                       /* a NaN quotient encodes as 0x7F */
                 bs = orc_e4m3_encode(orc_rn_f32(bamax / den));
             double sc = orc_rn_f32(orc_e4m3_decode(bs) * tsd);
             sf[r * nb + b] = bs;
@@ -312,7 +320,7 @@ void orc_pack(const uint16_t *y, int64_t ldy, int64_t m, int64_t m_pad, int64_t 
                 uint8_t c[2];
                 for (int t = 0; t < 2; ++t) {
                     double yv = v[j + t];
-                    if (sc == 0.0)
+                    if (sc == 0.0 || sc != sc)      /* zero or NaN scale product: signed zeros */
                         c[t] = signbit(yv) ? 0x8 : 0x0;
                     else
                         c[t] = orc_e2m1_encode(orc_rn_f32(yv / sc));

@@ -175,12 +175,48 @@ def test_all_zero_tensor(h3):
     assert ts == 0.0
 
 
-def test_nan_input_gives_nan_scale_without_error(h3):
-    m, d = 20, 256
+def _same_scale(ts, ts_o):
+    """Equal tensor scales: the same bits, or both NaN (the payload is not specified)."""
+    return (np.isnan(ts) and np.isnan(ts_o)) or _f32_bits(ts) == _f32_bits(ts_o)
+
+
+NON_FINITE = {"nan": 0x7FC0, "neg_nan": 0xFFC0, "inf": 0x7F80, "neg_inf": 0xFF80}
+
+
+@pytest.mark.parametrize("kind", list(NON_FINITE))
+def test_non_finite_inputs_bit_exact(h3, kind):
+    """A NaN or an infinity in the input: the tensor scale is NaN or infinite and
+    the oracle's stated conventions decide the bytes (a NaN quotient is the
+    E4M3 NaN code 0x7F, a zero or NaN scale product gives signed zeros); the
+    modulation producer, the plain producer and the SwiGLU producer (with and
+    without the h workspace) must match them byte for byte."""
+    v = NON_FINITE[kind]
+    m, d = 40, 512
     x, sh, sc = _random_case(m, d, 1, seed=14)
-    x[4, 9] = 0x7FC0
-    ts, _, _ = run_modulate(h3, x, sh, sc, [0, m], 32)
-    assert np.isnan(ts)
+    sh[:] = 0                                # keep the planted value through the modulation
+    x[4, 9] = v
+    x[7, 16:32] = 0                          # an all-zero block
+    x[7, 40] = 0x8000
+    x[11, 64:80] = v                         # a block of nothing but the planted value
+    ts_o, q_o, sf_o, _, _ = oracle.modulate_producer(x, sh, sc, [0, m], 48)
+    ts, q, sfa = run_modulate(h3, x, sh, sc, [0, m], 48)
+    assert np.isnan(ts_o) if "nan" in kind else np.isinf(ts_o)
+    assert _same_scale(ts, ts_o), (ts, ts_o)
+    assert np.array_equal(q, q_o), f"QDATA differs at {np.argwhere(q != q_o)[:5].tolist()}"
+    assert np.array_equal(sfa, oracle.swizzle_sf(sf_o))
+    assert (sf_o[:m] == 0x7F).any() and not q_o[:m][q_o[:m] & 0x77 != 0].any()
+
+    ts_o, q_o, sf_o, _ = oracle.plain_producer(x, 48)
+    ts, q, sfa = run_plain(h3, x, 48)
+    assert _same_scale(ts, ts_o) and np.array_equal(q, q_o) and np.array_equal(sfa, oracle.swizzle_sf(sf_o))
+
+    g = _bf16(torch.randn(m, d, generator=torch.Generator().manual_seed(15)))
+    u = x.copy()                             # h = silu(g) * u carries the planted value
+    ts_o, q_o, sf_o, h_o, _ = oracle.swiglu_producer(g, u, 48)
+    for workspace in (False, True):
+        ts, q, sfa, h = run_swiglu(h3, g, u, 48, workspace)
+        assert _same_scale(ts, ts_o), (workspace, ts, ts_o)
+        assert np.array_equal(q, q_o) and np.array_equal(sfa, oracle.swizzle_sf(sf_o)), workspace
 
 
 def test_leading_dimensions(h3):

@@ -279,6 +279,52 @@ def test_pack_tiny_adversarial_properties():
     assert (sf[[30, 31, 280]] == 0).sum() >= 4                 # scales that round to zero
 
 
+def _codes(q, m):
+    lo, hi = q[:m] & 0xF, q[:m] >> 4
+    return np.stack([lo, hi], -1).reshape(m, -1)
+
+
+def test_pack_non_finite_inputs_hand_derived():
+    """NaN and infinity, by hand from the formulas in IEEE arithmetic and the
+    two stated conventions (a NaN quotient is the E4M3 NaN code 0x7F; a zero
+    or NaN scale product gives zeros with y's signs).
+
+    NaN tensor: amax and ts are NaN, so every block with a nonzero maximum has
+    quotient NaN -> 0x7F and an all-zero block keeps 0; every scale product
+    (NaN * anything, 0 * NaN) is NaN, so every code is a signed zero.
+    Infinite tensor: ts = RN(inf / 2688) = inf; the block holding the infinity
+    has quotient inf / inf = NaN -> 0x7F, a finite nonzero block has
+    quotient 0 -> 0, and every scale product (NaN * inf, 0 * inf) is NaN."""
+    nan, pinf, neg_zero = 0x7FC0, 0x7F80, 0x8000
+    one, two, mthree = 0x3F80, 0x4000, 0xC040
+    y = np.zeros((2, 64), dtype=np.uint16)
+    y[0, 0:16] = one
+    y[0, 3] = nan                        # block 0: NaN among finite values
+    y[0, 16:32] = 0
+    y[0, 20] = neg_zero                  # block 1: all zero (one -0)
+    y[0, 32:48] = mthree                 # block 2: finite, negative
+    y[0, 48:64] = nan | 0x8000           # block 3: negative NaNs only
+    y[1, :] = two
+    ts = oracle.tensor_scale(oracle.absmax(y))
+    assert np.isnan(ts)
+    q, sf = oracle.pack(y, 16, ts)
+    assert sf[0].tolist() == [0x7F, 0x00, 0x7F, 0x7F] and sf[1].tolist() == [0x7F] * 4
+    want = np.where(y.view(np.int16) < 0, 8, 0)      # zeros with y's signs
+    assert np.array_equal(_codes(q, 2), want)
+    assert not q[2:].any() and not sf[2:].any()
+
+    y = np.zeros((1, 48), dtype=np.uint16)
+    y[0, 0:16] = one
+    y[0, 5] = pinf                       # block 0 holds +inf
+    y[0, 16:32] = mthree                 # block 1 finite
+    y[0, 40] = neg_zero                  # block 2 all zero
+    ts = oracle.tensor_scale(oracle.absmax(y))
+    assert ts == float("inf")
+    q, sf = oracle.pack(y, 16, ts)
+    assert sf[0].tolist() == [0x7F, 0x00, 0x00]
+    assert np.array_equal(_codes(q, 1), np.where(y.view(np.int16) < 0, 8, 0))
+
+
 # ---------------------------------------------------------------------------
 # Scale layout
 # ---------------------------------------------------------------------------
