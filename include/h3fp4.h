@@ -41,6 +41,12 @@
  *    bs  = E4M3_RNE_sat(RN_f32(block_amax / RN_f32(6 * ts)))   (0 if block_amax == 0)
  *    q   = E2M1_RNE_sat(RN_f32(y / RN_f32(dec(bs) * ts)))      (signed 0 if that product is 0)
  *    C   = RN_bf16(RN_f32(ts_a * ts_b) * sum_k a_k b_k)        (FP32 accumulation)
+ * Non-finite inputs follow the same formulas in IEEE arithmetic: a NaN makes
+ * its block maximum, amax and ts NaN, an infinity makes ts infinite; a NaN
+ * quotient encodes as the E4M3 NaN code 0x7F and a NaN scale product, like a
+ * zero one, gives zeros with y's signs.  So a tensor holding a NaN or an
+ * infinity packs to signed-zero codes with scale 0x7F on its non-zero blocks
+ * (0 on blocks whose quotient is 0), and any GEMM over it is NaN.
  */
 #ifndef H3FP4_H
 #define H3FP4_H
