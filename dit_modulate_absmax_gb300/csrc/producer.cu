@@ -178,36 +178,62 @@ struct ModulateSrc {
     SegTable seg;
 
     using Raw = Vec16;
-    struct State {
-        int64_t begin, end;  // rows of the segment whose parameters are loaded
-        uint32_t s1[8], sh[8];
+
+    // The CTA's copy of the modulation parameters for the current tile's 256
+    // columns: s1 = RN_bf16(scale + 1) and shift of every segment that the
+    // tile's rows touch, as [segment][column half of a 16-column block][block]
+    // (4 words each), and the segment of each of the tile's rows.  (Each
+    // thread keeping its 16 parameter words and its segment's row range in
+    // registers instead cost ~60 instructions per 16-value block of the pack
+    // under the 64-register budget of 4 CTAs per SM.)
+    struct Smem {
+        uint4 s1[H3FP4_MAX_SEGMENTS][2][kTileCols / kBlock];
+        uint4 sh[H3FP4_MAX_SEGMENTS][2][kTileCols / kBlock];
+        int32_t row_seg[kTileRows];
     };
 
-    __device__ __forceinline__ void begin(State &st) const
+    // Every thread of the CTA calls this for a tile whose first row row0 < m
+    // and first column c0; it begins and ends with a barrier.
+    __device__ __forceinline__ void stage(Smem &sm, int64_t row0, int64_t m, int c0) const
     {
-        st.begin = 1;
-        st.end = 0;  // empty range: the first row loads its segment
+        __syncthreads();   // the previous tile's readers are done with sm
+        if (threadIdx.x < kTileRows) {
+            // rows past m are never modulated; they take row m-1's segment
+            const int64_t r = min(row0 + static_cast<int64_t>(threadIdx.x), m - 1);
+            int64_t b, e;
+            sm.row_seg[threadIdx.x] = segment_of(seg, r, b, e);
+        }
+        __syncthreads();
+        const int first = sm.row_seg[0], count = sm.row_seg[kTileRows - 1] - first + 1;   // monotone in r
+        for (int i = threadIdx.x; i < 64 * count; i += kThreads) {
+            const int sg = first + (i >> 6), k = i & 63, chunk = k & 31;   // columns c0 + 8 chunk .. + 7
+            if (k < 32) {
+                uint4 v = ld16(scale + sg * ld_mod + c0 + 8 * chunk);
+                const uint32_t one2 = 0x3F803F80u;   // bf16 1.0 in both halves
+                v = make_uint4(bf2_add(v.x, one2), bf2_add(v.y, one2), bf2_add(v.z, one2), bf2_add(v.w, one2));
+                sm.s1[sg][chunk & 1][chunk >> 1] = v;
+            } else {
+                sm.sh[sg][chunk & 1][chunk >> 1] = ld16(shift + sg * ld_mod + c0 + 8 * chunk);
+            }
+        }
+        __syncthreads();
     }
     __device__ __forceinline__ Raw load(int64_t r, int col) const { return ld32(x + r * ldx + col); }
 
-    // y = RN_bf16(RN_bf16(x * RN_bf16(scale + 1)) + shift), per segment of row r.
-    __device__ __forceinline__ void apply(State &st, int64_t r, int col, const Raw &raw, uint32_t (&y)[8]) const
+    // y = RN_bf16(RN_bf16(x * RN_bf16(scale + 1)) + shift) for the tile's row rr
+    // (segment from the table) and 16-column block blk.
+    __device__ __forceinline__ void apply(const Smem &sm, int rr, int blk, const Raw &raw, uint32_t (&y)[8]) const
     {
-        if (r < st.begin || r >= st.end) {
-            const int s = segment_of(seg, r, st.begin, st.end);
-            uint32_t sc[8];
-            words(ld32(scale + s * ld_mod + col), sc);
-            words(ld32(shift + s * ld_mod + col), st.sh);
-            const uint32_t one2 = 0x3F803F80u;  // bf16 1.0 in both halves
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                st.s1[i] = bf2_add(sc[i], one2);
-        }
+        const int sg = sm.row_seg[rr];
+        const uint4 a0 = sm.s1[sg][0][blk], a1 = sm.s1[sg][1][blk];
+        const uint4 b0 = sm.sh[sg][0][blk], b1 = sm.sh[sg][1][blk];
+        const uint32_t s1[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t sh[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
         uint32_t xw[8];
         words(raw, xw);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            y[i] = bf2_add(bf2_mul(xw[i], st.s1[i]), st.sh[i]);
+            y[i] = bf2_add(bf2_mul(xw[i], s1[i]), sh[i]);
     }
     __device__ __forceinline__ void keep(int64_t, int, const uint32_t (&)[8]) const {}
 };
@@ -224,16 +250,16 @@ struct SwigluSrc {
     struct Raw {
         Vec16 g, u;
     };
-    struct State {};
+    struct Smem {};
 
-    __device__ __forceinline__ void begin(State &) const {}
+    __device__ __forceinline__ void stage(Smem &, int64_t, int64_t, int) const {}
     __device__ __forceinline__ Raw load(int64_t r, int col) const
     {
         return Raw{ld32(g + r * ldg + col), ld32(u + r * ldu + col)};
     }
 
     // h = RN_bf16(silu_bf16(gate) * up).
-    __device__ __forceinline__ void apply(State &, int64_t, int, const Raw &raw, uint32_t (&y)[8]) const
+    __device__ __forceinline__ void apply(const Smem &, int, int, const Raw &raw, uint32_t (&y)[8]) const
     {
         uint32_t gw[8], uw[8], sv[8];
         words(raw.g, gw);
@@ -276,10 +302,10 @@ struct PlainSrc {  // already-materialised bf16 values (SwiGLU pass 2 with a wor
     int64_t ldh;
 
     using Raw = Vec16;
-    struct State {};
-    __device__ __forceinline__ void begin(State &) const {}
+    struct Smem {};
+    __device__ __forceinline__ void stage(Smem &, int64_t, int64_t, int) const {}
     __device__ __forceinline__ Raw load(int64_t r, int col) const { return ld32(h + r * ldh + col); }
-    __device__ __forceinline__ void apply(State &, int64_t, int, const Raw &raw, uint32_t (&y)[8]) const
+    __device__ __forceinline__ void apply(const Smem &, int, int, const Raw &raw, uint32_t (&y)[8]) const
     {
         words(raw, y);
     }
@@ -338,19 +364,19 @@ __device__ __forceinline__ uint32_t absmax16(const uint32_t (&y)[8])
 // Pass 1 over the tiles blockIdx.x, blockIdx.x + gridDim.x, ...: this thread's
 // maximum |y| bit pattern (the values are also kept by Src, e.g. h).
 template <class Src>
-__device__ __forceinline__ uint32_t absmax_tiles(const Src &src, int64_t m, int col_tiles, int64_t n_tiles)
+__device__ __forceinline__ uint32_t absmax_tiles(const Src &src, int64_t m, int col_tiles, int64_t n_tiles,
+                                                typename Src::Smem &ssm)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane & 15, half = lane >> 4;
-    typename Src::State st;
     uint32_t vmax = 0;
-    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {   // the same count in every thread of the CTA
         int64_t row_tile;
         int col_tile;
         tile_rc(t, col_tiles, row_tile, col_tile);
         const int64_t row0 = row_tile * kTileRows;
         const int col = col_tile * kTileCols + sub * kBlock;
-        src.begin(st);  // cached per-column parameters belong to the previous tile's columns
+        src.stage(ssm, row0, m, col_tile * kTileCols);   // every tile here has rows below m
 #pragma unroll 1
         for (int i0 = 0; i0 < kSteps; i0 += kUnroll) {
             typename Src::Raw raw[kUnroll];
@@ -365,7 +391,7 @@ __device__ __forceinline__ uint32_t absmax_tiles(const Src &src, int64_t m, int 
                 const int64_t r = row0 + kRowsPerStep * (i0 + u) + 2 * warp + half;
                 if (r < m) {
                     uint32_t y[8];
-                    src.apply(st, r, col, raw[u], y);
+                    src.apply(ssm, kRowsPerStep * (i0 + u) + 2 * warp + half, sub, raw[u], y);
                     src.keep(r, col, y);
                     vmax = max(vmax, absmax16(y));
                 }
@@ -403,7 +429,8 @@ template <class Src>
 __global__ void __launch_bounds__(kThreads, min_blocks<Src>()) absmax_kernel(Src src, int64_t m, int col_tiles, int64_t n_tiles,
                                                           uint32_t *scratch, float *ts_out)
 {
-    const uint32_t mx = cta_max(absmax_tiles(src, m, col_tiles, n_tiles));
+    __shared__ typename Src::Smem ssm;
+    const uint32_t mx = cta_max(absmax_tiles(src, m, col_tiles, n_tiles, ssm));
     if (threadIdx.x == 0) {
         atomicMax(&scratch[0], mx);
         __threadfence();
@@ -518,7 +545,7 @@ __device__ __forceinline__ uint2 encode16(const uint32_t (&y)[8], float sc)
 template <class Src>
 __device__ __forceinline__ void pack_tile(const Src &src, int64_t t, int64_t m, int64_t m_pad, int64_t d,
                                           int col_tiles, float ts, float den, float rden, bool den_fma,
-                                          uint8_t *qdata, uint8_t *sf, uint8_t *sft)
+                                          uint8_t *qdata, uint8_t *sf, uint8_t *sft, typename Src::Smem &ssm)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane & 15, half = lane >> 4;
@@ -528,8 +555,8 @@ __device__ __forceinline__ void pack_tile(const Src &src, int64_t t, int64_t m, 
     const int64_t row0 = row_tile * kTileRows;
     const int col = col_tile * kTileCols + sub * kBlock;
     const int64_t qld = d / 2;
-    typename Src::State st;
-    src.begin(st);
+    if (row0 < m)   // the same in every thread of the CTA
+        src.stage(ssm, row0, m, col_tile * kTileCols);
 
 #pragma unroll 1
     for (int i0 = 0; i0 < kSteps; i0 += kUnroll) {
@@ -546,7 +573,7 @@ __device__ __forceinline__ void pack_tile(const Src &src, int64_t t, int64_t m, 
             const int64_t r = row0 + rr;
             uint32_t y[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
             if (r < m)
-                src.apply(st, r, col, raw[u], y);
+                src.apply(ssm, rr, sub, raw[u], y);
             // bs = E4M3_RNE_sat(RN_f32(block_amax / RN_f32(6 ts))); an all-zero block gets 0.
             const uint32_t bs = block_scale(absmax16(y), den, rden, den_fma);
             const float sc = __fmul_rn(e4m3_value(bs), ts);
@@ -588,9 +615,10 @@ __global__ void __launch_bounds__(kThreads, min_blocks<Src>()) pack_kernel(Src s
                                                         uint8_t *sf)
 {
     __shared__ __align__(16) uint8_t sft[4 * 512];
+    __shared__ typename Src::Smem ssm;
     const PackConsts c = pack_consts(*ts_ptr);
     pack_tile(src, n_tiles - 1 - blockIdx.x, m, m_pad, d, col_tiles, c.ts, c.den, c.rden, c.den_fma, qdata, sf,
-              sft);
+              sft, ssm);
 }
 
 // ---------------------------------------------------------------------------
@@ -620,7 +648,11 @@ __global__ void __launch_bounds__(kThreads, min_blocks<Src1>())
     __shared__ float ts_sh;
     __shared__ int ok_sh;
     __shared__ uint32_t claim_sh[2];
-    const uint32_t mx = cta_max(absmax_tiles(src1, m, col_tiles, n_tiles1));
+    __shared__ union {   // pass 1's parameter copy, then pass 2's (a barrier lies between)
+        typename Src1::Smem p1;
+        typename Src2::Smem p2;
+    } ssm;
+    const uint32_t mx = cta_max(absmax_tiles(src1, m, col_tiles, n_tiles1, ssm.p1));
     if (threadIdx.x == 0) {
         atomicMax(&scratch[0], mx);
         __threadfence();
@@ -665,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<Src1>())
         if (threadIdx.x == 0)
             claim_sh[slot ^ 1] = atomicAdd(&scratch[1], 1u) - gridDim.x;
         pack_tile(src2, n_tiles2 - 1 - static_cast<int64_t>(idx), m, m_pad, d, col_tiles, c.ts, c.den, c.rden,
-                  c.den_fma, qdata, sf, sft);
+                  c.den_fma, qdata, sf, sft, ssm.p2);
         __syncthreads();   // sft and the claim slot just read are reused by the next tile
         slot ^= 1;
     }
