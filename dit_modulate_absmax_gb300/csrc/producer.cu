@@ -313,15 +313,25 @@ struct PlainSrc {  // already-materialised bf16 values (SwiGLU pass 2 with a wor
 };
 
 // Resident CTAs per SM that a kernel reading values from Src is compiled for
-// (the register budget): more warps hide more memory latency, until spills
-// cost more than that gains.  Measured at 37,810 rows: the modulation passes
-// 3 -> 4 per SM 6 % faster and 5 slower (the pack pass then spills ~200
-// bytes); the SwiGLU and plain single-launch producers 3 -> 4 -> 5 per SM
-// 0.806 -> 0.770 -> 0.747 ms and 0.251 -> 0.237 -> 0.232 ms.
+// (the register budget), and rows in flight per thread in pass 1: more warps
+// and more loads in flight hide more memory latency, until spills cost more
+// than that gains.  Measured at 37,810 x 7,168 (L2 flushed; the modulation
+// parameters staged in shared memory): modulation pass 1 at 4 CTAs per SM
+// 0.100 ms with 4 rows in flight, 0.102 with 2, 0.110 at 5 CTAs with 2;
+// modulation pass 2 (2 rows in flight) 0.131 ms at 5 CTAs per SM, 0.137 at
+// 4, 0.143 at 3 with 4 rows; the SwiGLU and plain single-launch producers
+// 3 -> 4 -> 5 per SM 0.806 -> 0.770 -> 0.747 ms and 0.251 -> 0.237 -> 0.232 ms.
 template <class Src>
 constexpr int min_blocks()
 {
     return Src::kModulated ? 4 : 5;
+}
+constexpr int kPackMinBlocks = 5;   // pass 2 alone (pack_kernel), every source
+
+template <class Src>
+constexpr int pass1_unroll()
+{
+    return Src::kModulated ? 4 : kUnroll;
 }
 
 // Row tile and column tile of tile t (column tiles fastest).  A 32-bit
@@ -378,16 +388,17 @@ __device__ __forceinline__ uint32_t absmax_tiles(const Src &src, int64_t m, int 
         const int col = col_tile * kTileCols + sub * kBlock;
         src.stage(ssm, row0, m, col_tile * kTileCols);   // every tile here has rows below m
 #pragma unroll 1
-        for (int i0 = 0; i0 < kSteps; i0 += kUnroll) {
-            typename Src::Raw raw[kUnroll];
+        constexpr int kU = pass1_unroll<Src>();
+        for (int i0 = 0; i0 < kSteps; i0 += kU) {
+            typename Src::Raw raw[kU];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < kU; ++u) {
                 const int64_t r = row0 + kRowsPerStep * (i0 + u) + 2 * warp + half;
                 if (r < m)
                     raw[u] = src.load(r, col);
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < kU; ++u) {
                 const int64_t r = row0 + kRowsPerStep * (i0 + u) + 2 * warp + half;
                 if (r < m) {
                     uint32_t y[8];
@@ -610,7 +621,7 @@ __device__ __forceinline__ PackConsts pack_consts(float ts)
 // Pass 2: one CTA per 128 x 256 tile (tiles visited in reverse order).
 // ---------------------------------------------------------------------------
 template <class Src>
-__global__ void __launch_bounds__(kThreads, min_blocks<Src>()) pack_kernel(Src src, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
+__global__ void __launch_bounds__(kThreads, kPackMinBlocks) pack_kernel(Src src, int64_t m, int64_t m_pad, int64_t d, int col_tiles,
                                                         int64_t n_tiles, const float *ts_ptr, uint8_t *qdata,
                                                         uint8_t *sf)
 {
