@@ -387,8 +387,8 @@ __device__ __forceinline__ uint32_t absmax_tiles(const Src &src, int64_t m, int 
         const int64_t row0 = row_tile * kTileRows;
         const int col = col_tile * kTileCols + sub * kBlock;
         src.stage(ssm, row0, m, col_tile * kTileCols);   // every tile here has rows below m
-#pragma unroll 1
         constexpr int kU = pass1_unroll<Src>();
+#pragma unroll 1
         for (int i0 = 0; i0 < kSteps; i0 += kU) {
             typename Src::Raw raw[kU];
 #pragma unroll
