@@ -136,3 +136,36 @@ def test_model_width_attention_output_linear(h3):
     wt, C = _gemm(h3, w, q, sfa, ts, dev)
     ts_o, q_o, sf_o = _check_producer_all_rows(w, _u16(act["x"]), ts, q, sfa)
     _check_gemm_rows(w, q_o, sf_o, ts_o, wt, C, seed=34)
+
+
+def test_model_width_fc2_gated_residual_in_place_full_size(h3):
+    """The model-width FC2 (37,810 x 5,376 x 14,336) through the gated residual
+    epilogue ("NVFP4 Streaming Design", P4), written in place over the residual
+    with two gate segments split at row 32,768, in the benchmark's launch form:
+    whole 256-row tiles (first, last, both sides of the split) and random rows,
+    every column, within the bounds the oracle derives from its FP64 sums."""
+    w = W.WORKLOADS["h3_fc2"]
+    dev = torch.device("cuda")
+    act = W.activations(w, device=dev)
+    ts, q, sfa = h3.swiglu_pack(act["gate"], act["up"], w.m_pad)
+    wt = W.weights(w, device=dev)
+    bsf = h3.swizzle_scales(wt["sf"][: w.n])
+    bts = torch.tensor([wt["ts"]], dtype=torch.float32, device=dev)
+    g = torch.Generator().manual_seed(36)
+    gate = torch.randn(2, w.n, generator=g).to(torch.bfloat16).view(torch.int16)
+    res = (torch.randn(w.m, w.n, generator=g) * 4).to(torch.bfloat16).view(torch.int16)
+    off = [0, 32_768, w.m]
+    out = res.to(dev)
+    h3.gemm_gated_residual(q, sfa, ts, wt["q"], bsf, bts, w.m, gate.to(dev), off, out, out=out)
+    torch.cuda.synchronize()
+    assert h3.h3fp4_device_error() == 0
+    ts_o, q_o, sf_o = _check_producer_all_rows(w, oracle.swiglu(_u16(act["gate"]), _u16(act["up"])), ts, q, sfa)
+    rows = _gemm_rows(w.m, seed=37)
+    R, S = oracle.gemm_reference(q_o, sf_o, ts_o, wt["q"].cpu().numpy(), wt["sf"].cpu().numpy(), wt["ts"], w.k,
+                                 rows=rows)
+    res_rows = res.numpy().view(np.uint16)[rows]
+    split = int((rows < 32_768).sum())
+    lo, hi = oracle.gated_residual_bounds(R, S, gate.numpy().view(np.uint16), [0, split, len(rows)], res_rows)
+    got = oracle.bf16_to_f64(_u16(out[torch.from_numpy(rows).to(dev)]))
+    bad = np.argwhere((got < lo) | (got > hi))
+    assert bad.size == 0, f"{len(bad)} outputs outside the bounds, first {bad[:4].tolist()}"
