@@ -618,8 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTAs' TMEM slot for the stage (each CTA's shared memory into its own TMEM),
 // each committing to the same full barrier, which therefore completes once
 // A and B have landed and the scales are in TMEM (3 arrivals: the producer's
-// expect-tx and the two commits); the MMA warp waits for it, issues the 4
-// pair MMAs and commits the stage free in both CTAs.  These
+// expect-tx and the two commits); the MMA warp waits for it, issues the
+// stage's three pair MMAs (K = 96, 96, 64) and commits the stage free in both
+// CTAs.  These
 // warps run their loops warp-collectively, each tcgen05 instruction issued by
 // one elected lane.  What the tensor pipe waits on is the issuing warps'
 // per-stage time (a satisfied barrier wait alone costs ~100 cycles, a tcgen05
