@@ -170,6 +170,7 @@ __device__ __forceinline__ void words(const Vec16 &v, uint32_t (&w)[8])
 
 struct ModulateSrc {
     static constexpr bool kModulated = true;
+    static constexpr int kPass1Unroll = 4;   // rows in flight per thread in pass 1
     const uint16_t *x;
     int64_t ldx;
     const uint16_t *shift;
@@ -240,6 +241,7 @@ struct ModulateSrc {
 
 struct SwigluSrc {
     static constexpr bool kModulated = false;
+    static constexpr int kPass1Unroll = 1;
     const uint16_t *g;
     int64_t ldg;
     const uint16_t *u;
@@ -298,6 +300,7 @@ struct SwigluSrc {
 
 struct PlainSrc {  // already-materialised bf16 values (SwiGLU pass 2 with a workspace)
     static constexpr bool kModulated = false;
+    static constexpr int kPass1Unroll = kUnroll;
     const uint16_t *h;
     int64_t ldh;
 
@@ -320,7 +323,10 @@ struct PlainSrc {  // already-materialised bf16 values (SwiGLU pass 2 with a wor
 // 0.100 ms with 4 rows in flight, 0.102 with 2, 0.110 at 5 CTAs with 2;
 // modulation pass 2 (2 rows in flight) 0.131 ms at 5 CTAs per SM, 0.137 at
 // 4, 0.143 at 3 with 4 rows; the SwiGLU and plain single-launch producers
-// 3 -> 4 -> 5 per SM 0.806 -> 0.770 -> 0.747 ms and 0.251 -> 0.237 -> 0.232 ms.
+// 3 -> 4 -> 5 per SM 0.806 -> 0.770 -> 0.747 ms and 0.251 -> 0.237 -> 0.232 ms
+// (the SwiGLU producer at 4 and 6 per SM 0.734 and 0.752 ms against 0.722 at
+// 5; with 1 row in flight in pass 1, whose two inputs fill the registers
+// that a second row would need, 0.714 ms).
 template <class Src>
 constexpr int min_blocks()
 {
@@ -331,7 +337,7 @@ constexpr int kPackMinBlocks = 5;   // pass 2 alone (pack_kernel), every source
 template <class Src>
 constexpr int pass1_unroll()
 {
-    return Src::kModulated ? 4 : kUnroll;
+    return Src::kPass1Unroll;
 }
 
 // Row tile and column tile of tile t (column tiles fastest).  A 32-bit
