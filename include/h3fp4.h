@@ -69,7 +69,7 @@ typedef enum h3fp4_status {
     H3FP4_ERR_NULL = 1,        /* a required pointer is NULL */
     H3FP4_ERR_ALIGN = 2,       /* a pointer or leading dimension breaks the 16-byte rule */
     H3FP4_ERR_SHAPE = 3,       /* a size is negative, too large, or not a required multiple */
-    H3FP4_ERR_UNSUPPORTED = 4, /* a configuration this build does not implement */
+    H3FP4_ERR_UNSUPPORTED = 4, /* a configuration the library does not implement */
     H3FP4_ERR_CUDA = 5,        /* a CUDA call failed (see cudaGetLastError) */
     H3FP4_ERR_DEVICE = 6       /* a kernel recorded a device-side error (bounded wait ran out) */
 } h3fp4_status;

@@ -1,4 +1,4 @@
-"""bench.py's multi-rank path on CPU: N replicas (one per GPU on a GPU machine),
+"""bench.py's multi-rank path on CPU: N replicas (one per GPU),
 timed as the slowest rank, whole-job ms per linear over all ranks' linears.
 Two gloo ranks on 127.0.0.1 stand in for two GPUs, each running its own CPU
 stand-in of a step through the same timed region the GPU path uses; nothing
