@@ -35,7 +35,8 @@ namespace {
 
 // kSiluLut: uint16[65536], the correctly rounded bf16 silu of every bf16
 // pattern (generated at build time); used where the FP32 evaluation below is
-// too close to a bf16 rounding boundary, and for g < -80 and NaN.
+// too close to a bf16 rounding boundary, and for g < -16, |g| < 2^-100 and
+// NaN (silu_needs_table).
 #include "silu_lut.inc"
 
 constexpr int kTileRows = 128;
